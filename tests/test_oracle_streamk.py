@@ -1,0 +1,114 @@
+"""Pins for the work-split definitions (CPU only): the pages' two worked
+examples (tests/golden/) plus invariants and brute-force enumeration."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import streamk as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def test_four_sm_timeline_from_the_waves_page():
+    g = _golden("waves_4sm_8task_timeline.json")
+    r = S.list_schedule(g["task_times_ms"], g["n_workers"])
+    assert [list(t) for t in r["tasks"]] == g["expected"]["tasks"]
+    assert r["makespan"] == g["expected"]["makespan_ms"]
+    assert r["idle"] == g["expected"]["idle_ms_per_sm"]
+    loads = S.streamk_loads(g["task_times_ms"], g["n_workers"])
+    assert loads == g["one_wave_equal_split"]["per_sm_ms"]
+    assert max(loads) == g["one_wave_equal_split"]["makespan_ms"]
+
+
+def test_streamk_split_on_the_timeline_tasks():
+    """The same 8 tasks as work items of one kv head (granule 1 ms): the one-wave
+    split gives every SM exactly 155 units."""
+    g = _golden("waves_4sm_8task_timeline.json")
+    r = S.streamk_split(g["task_times_ms"], 1, 4, granule=1)
+    per = [sum(te - tb for _, tb, te in segs) for segs in r["segments"]]
+    assert per == [155, 155, 155, 155]
+
+
+def test_megartp_round_robin_queue_fill():
+    g = _golden("megartp_round_robin_queues.json")
+    q = S.round_robin_queues(g["n_tasks"], g["n_queues"])
+    valid = (q >= 0).sum(axis=1)
+    assert list(q.shape) == g["expected"]["padded_shape"]
+    assert int((valid == 5).sum()) == g["expected"]["queues_with_5"]
+    assert int((valid == 4).sum()) == g["expected"]["queues_with_4"]
+    assert int((q < 0).sum()) == g["expected"]["noop_slots"]
+    assert sorted(q[q >= 0].tolist()) == list(range(g["n_tasks"]))
+
+
+def _brute_force_split(seqlens, hkv, n, granule):
+    """Enumerate every granule of every item, deal contiguous index ranges."""
+    units = []
+    for b, L in enumerate(seqlens):
+        for h in range(hkv):
+            for u in range(-(-L // granule)):
+                units.append((b * hkv + h, u))
+    total = len(units)
+    out = []
+    for c in range(n):
+        lo, hi = c * total // n, (c + 1) * total // n
+        segs = {}
+        for item, u in units[lo:hi]:
+            segs.setdefault(item, []).append(u)
+        row = []
+        for item in sorted(segs):
+            us = segs[item]
+            L = seqlens[item // hkv]
+            row.append((item, min(us) * granule, min((max(us) + 1) * granule, L)))
+        out.append(row)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_streamk_split_matches_brute_force_and_invariants(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 7))
+    hkv = int(rng.integers(1, 4))
+    n = int(rng.integers(1, 12))
+    granule = int(rng.choice([1, 4, 16]))
+    seqlens = [int(x) for x in rng.integers(0, 120, size=B)]
+    if seed % 5 == 0:
+        seqlens[0] = 0
+    r = S.streamk_split(seqlens, hkv, n, granule)
+    bf = _brute_force_split(seqlens, hkv, n, granule)
+    nonempty = [[s for s in segs if s[2] > s[1]] for segs in r["segments"]]
+    assert nonempty == bf
+    # every token of every item covered exactly once, splits in order
+    for i, splits in enumerate(r["item_splits"]):
+        L = seqlens[i // hkv]
+        if L == 0:
+            assert len(splits) == 1 and splits[0][1:] == (0, 0)
+            continue
+        edges = [(tb, te) for _, tb, te in splits]
+        assert edges[0][0] == 0 and edges[-1][1] == L
+        assert all(a[1] == b[0] for a, b in zip(edges, edges[1:]))
+        ctas = [c for c, _, _ in splits]
+        assert ctas == sorted(ctas) and len(set(ctas)) == len(ctas)
+    # near-equal chunks: granule counts differ by at most one
+    per = [sum(-(-(te - tb) // granule) if te > tb else 0 for _, tb, te in segs)
+           for segs in r["segments"]]
+    b = r["bounds"]
+    assert per == [b[c + 1] - b[c] for c in range(n)]
+    assert max(per) - min(per) <= 1
+    nseg = sum(len(s) for s in r["segments"])
+    assert nseg <= B * hkv + n - 1 + sum(1 for L in seqlens if L == 0) * hkv
+    # segments of a CTA are in item order
+    for segs in r["segments"]:
+        items = [s[0] for s in segs]
+        assert items == sorted(items)
+
+
+def test_round_robin_split_deals_whole_items():
+    r = S.round_robin_split([5, 0, 9], 2, 4)
+    assert r["segments"] == [[(0, 0, 5), (4, 0, 9)], [(1, 0, 5), (5, 0, 9)], [(2, 0, 0)], [(3, 0, 0)]]
