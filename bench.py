@@ -1,0 +1,395 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark: µs per call and achieved HBM TB/s on one GB300.
+
+A step is one decode-attention call over the whole batch of the workload (the
+Stream-K plan + one persistent kernel). Default workload: the Llama-3-8B-shaped
+GQA decode batch (B=32, 32 q / 8 kv heads, D=128, L ~ U[512, 8192], P=16).
+
+  value   algorithmic bytes / device time (CUDA events on the launching stream),
+          inputs resident in HBM; KV (~570 MB) is larger than L2, so no flush
+  e2e     the same metric through the public API with host buffers: per step the
+          host planner runs, q / seqlens / page table / plan are copied from
+          pinned host memory, and out / lse are copied back (KV cache resident)
+  roofline / cpu_baseline / clocks: see the design doc (measurement section)
+
+--impl reference times the fp64 CPU oracle on the host cores instead.
+Multi-GPU (torchrun): every rank runs an independent replica (weak scaling, no
+collective on the data path); value = all ranks' bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/call and achieved HBM TB/s (% of roofline) on 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = {"gqa": "sm_load_balancing_gb300/csrc/gqa_decode.cu",
+              "mla": "sm_load_balancing_gb300/csrc/mla_decode.cu"}
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b_gqa")
+    ap.add_argument("--mode", choices=["streamk", "round_robin"], default="streamk")
+    ap.add_argument("--n-ctas", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample (cpu_baseline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+    def find(o):
+        if isinstance(o, dict):
+            for k, v in o.items():
+                if k.lower() in ("hbm_gbs", "hbm_gb_s", "hbm_bandwidth_gbs") and isinstance(v, (int, float)):
+                    return float(v)
+                r = find(v)
+                if r:
+                    return r
+        return None
+    v = find(d)
+    return (v, "measured (MEASURED_PEAKS.json hbm_gbs)") if v else (FALLBACK_HBM_GBS, "fallback")
+
+
+def _traffic(kind, workload):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    src = os.path.join(ROOT, KERNEL_SRC[kind])
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        e = d.get(workload)
+        if e and e.get("kernel_src_sha256_16") == sha:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampler for the SM clock and throttle reasons."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [r.split(", ") for r in self.f.read().strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def _cpu_oracle_sample(w, target_s):
+    """Time the fp64 oracle on the first requests of the batch, about
+    `target_s` seconds of work. Returns (bytes_per_s, cores, description)."""
+    import numpy as np
+
+    from oracle import attention as A
+    A.build()
+    rows_per_req = w.q_tokens * w.num_q_heads
+    # probe one request to size the sample
+    order = list(range(w.batch))
+    t0 = time.perf_counter()
+    A.decode_workload(w, rows=list(range(rows_per_req)))
+    per_req = max(time.perf_counter() - t0, 1e-4) / max(int(w.seqlens[0]), 1)
+    budget_tokens = target_s / per_req
+    chosen, toks = [], 0
+    for b in order:
+        if chosen and toks + int(w.seqlens[b]) > budget_tokens:
+            break
+        chosen.append(b)
+        toks += int(w.seqlens[b])
+    rows = [b * rows_per_req + r for b in chosen for r in range(rows_per_req)]
+    t0 = time.perf_counter()
+    A.decode_workload(w, rows=rows)
+    dt = time.perf_counter() - t0
+    frac = toks / max(w.kv_tokens, 1)
+    sample_bytes = w.algorithmic_bytes() * frac
+    desc = (f"all {rows_per_req} query rows of requests 0..{chosen[-1]} "
+            f"({len(chosen)} of {w.batch} requests, {toks} of {w.kv_tokens} KV tokens), "
+            f"fp64 C oracle, OpenMP")
+    return sample_bytes / dt, A.num_threads(), desc, dt
+
+
+def run_reference(a):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import workloads as W
+    w = W.make(a.workload)
+    from oracle import attention as A
+    A.build()
+    # each step: a bounded sample of the workload (same rows every step)
+    per_step = max(0.5, min(10.0, 150.0 / max(a.steps + a.warmup, 1)))
+    for _ in range(a.warmup):
+        _cpu_oracle_sample(w, per_step * 0.2)
+    vals, times = [], []
+    desc, cores = "", 1
+    for _ in range(a.steps):
+        v, cores, desc, dt = _cpu_oracle_sample(w, per_step)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": 1e3 * w.algorithmic_bytes() / (value * 1e12),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
+        "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
+                   "l2": "CPU run"},
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def run_ours(a):
+    import numpy as np
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import sm_load_balancing_gb300 as skd
+    import workloads as W
+
+    w = W.make(a.workload, seed=rank)
+    kind = "mla" if w.mla else "gqa"
+
+    def bf16(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+
+    q = bf16(w.q).to(dev)
+    k = bf16(w.k_pages).to(dev)
+    v = None if w.mla else bf16(w.v_pages).to(dev)
+    pt = torch.from_numpy(w.page_table).to(dev)
+    sl = torch.from_numpy(w.seqlens).to(dev)
+    n = a.n_ctas or skd.sm_count()
+    shape = skd.make_shape(q, k, v, pt, scale=w.scale, causal=w.causal)
+    plan_h = skd.plan(w.seqlens, shape.num_kv_heads, w.page_size, n, a.mode)
+    plan_d = plan_h.to(dev)
+    ws = skd.workspace(shape, n, dev)
+    out = torch.empty(w.batch, w.q_tokens, w.num_q_heads, w.head_dim_v, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.batch, w.q_tokens, w.num_q_heads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        skd.decode_attention(q, k, v, pt, sl, plan_d, ws, scale=w.scale, causal=w.causal, n_ctas=n,
+                             out=out, lse=lse, shape=shape, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    if skd.read_error(ws) != 0:
+        raise RuntimeError(f"device error word {skd.read_error(ws)}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(a.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ck = clocks.stop()
+    total_ms = t_all0.elapsed_time(t_all1)
+    per = [s.elapsed_time(e) for s, e in ev]
+    mean_kernel_ms = sum(per) / len(per)
+    err = skd.read_error(ws)
+    if err != 0:
+        raise RuntimeError(f"device error word {err}")
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    alg_bytes = w.algorithmic_bytes()
+    ms_per_step = total_ms / a.steps
+    value = world * alg_bytes / (ms_per_step * 1e-3) / 1e12  # TB/s, all ranks
+
+    # ---- e2e through the public API with host buffers ----
+    e2e = None
+    if not a.no_e2e:
+        q_h = bf16(w.q).pin_memory()
+        pt_h = torch.from_numpy(w.page_table).pin_memory()
+        sl_h = torch.from_numpy(w.seqlens).pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        q_d, pt_d, sl_d = torch.empty_like(q), torch.empty_like(pt), torch.empty_like(sl)
+        plan_pin = torch.empty_like(plan_h).pin_memory()
+        plan_dd = torch.empty_like(plan_d)
+
+        def e2e_step():
+            p = skd.plan(sl_h, shape.num_kv_heads, w.page_size, n, a.mode)  # host planner
+            plan_pin.copy_(p)
+            q_d.copy_(q_h, non_blocking=True)
+            pt_d.copy_(pt_h, non_blocking=True)
+            sl_d.copy_(sl_h, non_blocking=True)
+            plan_dd.copy_(plan_pin, non_blocking=True)
+            skd.decode_attention(q_d, k, v, pt_d, sl_d, plan_dd, ws, scale=w.scale, causal=w.causal,
+                                 n_ctas=n, out=out, lse=lse, shape=shape, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(a.warmup):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        n_e2e = max(1, min(a.steps, 500))
+        for _ in range(n_e2e):
+            e2e_step()
+        t_e2e = (time.perf_counter() - t0) / n_e2e
+        barrier()
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([t_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        h2d = q_h.numel() * 2 + pt_h.numel() * 4 + sl_h.numel() * 4 + plan_pin.numel() * 4
+        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        e2e = {"value": world * alg_bytes / t_e2e / 1e12, "unit": "TB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "us_per_step": t_e2e * 1e6, "steps": n_e2e,
+               "note": "host planner + pinned H2D of q/seqlens/page table/plan + kernel + D2H of out/lse; KV cache resident"}
+        if skd.read_error(ws) != 0:
+            raise RuntimeError("device error in e2e loop")
+
+    peak, peak_src = _measured_hbm_peak()
+    achieved = alg_bytes / (mean_kernel_ms * 1e-3) / 1e9
+    traffic = _traffic(kind, w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_per_step, "us_per_call": ms_per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
+        "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
+                   "n_ctas": n, "plan": a.mode, "algorithmic_bytes": alg_bytes,
+                   "l2": "no flush: KV per step is larger than L2 (129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "kernel": f"{kind}_decode_kernel", "launch_ms_mean": mean_kernel_ms,
+                     "launch_ms_median": statistics.median(per)},
+        "e2e": e2e,
+        "gpu_launches": a.steps,
+        "clocks": ck,
+    }
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        try:
+            bps, cores, desc, dt = _cpu_oracle_sample(w, a.cpu_seconds)
+            line["cpu_baseline"] = {"value": bps / 1e12, "unit": "TB/s", "cores": cores,
+                                    "kind": "oracle", "sample": desc, "seconds": dt}
+        except Exception as ex:  # the bench line must still print
+            line["cpu_baseline"] = {"value": None, "unit": "TB/s", "cores": None, "kind": "oracle",
+                                    "sample": f"failed: {ex}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        return run_reference(a)
+    return run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

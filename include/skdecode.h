@@ -1,0 +1,177 @@
+/*
+ * skdecode -- Stream-K split-KV decode attention over a paged KV cache, for
+ * sm_103a (GB300). C ABI: plain pointers and sizes, no framework types.
+ *
+ * What the library computes (the passages it follows):
+ *   - attention itself: exact softmax attention, QK^T -> mask -> softmax -> xV,
+ *     streamed with an online softmax so no score matrix is written to HBM
+ *     ("GPU Kernel、异步 Launch、Stream 与融合 Kernel 全解", section 6.3 and Q8);
+ *   - the work split: the batch's KV tokens are cut into as many near-equal
+ *     chunks as there are CTAs and launched as one wave (triton.csdn.net Q&A
+ *     on waves and FlashMLA's Stream-K, closing summary);
+ *   - the reduction: partial softmax states of the splits of one (request,
+ *     kv head) are merged inside the same kernel as soon as the last split is
+ *     done -- no separate combine kernel and no wait for the slowest SM
+ *     ("MeldKernel：动态负载下跨 SM 融合内核（SOSP 2026）", key observations and
+ *     core method: just-in-time reduction);
+ *   - the split is chosen at run time from the real sequence lengths
+ *     (same page, core method).
+ *
+ * Conventions for every call
+ *   - The caller owns and allocates every buffer; the library allocates no
+ *     device memory. "device" pointers are CUDA global-memory addresses on the
+ *     current device; "host" pointers are ordinary CPU memory.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream. Calls that take a stream only enqueue work on it.
+ *   - Every call returns an skd_status (SKD_OK == 0) and never throws.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (2 bytes, little endian).
+ *
+ * Tensor layouts (row-major, all contiguous unless a stride is given)
+ *   q          bf16   [B][T][Hq][Dk]
+ *   k_pages    bf16   [NP][P][Hkv][Dk]           (token-major pages, "NHD")
+ *   v_pages    bf16   rows of Dv values; row (page, slot, kv head) starts at
+ *                     element ((page*P + slot)*Hkv + head) * v_row_stride.
+ *                     GQA: its own buffer [NP][P][Hkv][Dv], v_row_stride = Dv.
+ *                     MLA (absorbed): v_pages == k_pages, Hkv = 1,
+ *                     v_row_stride = Dk = 576, Dv = 512 (V = the first 512
+ *                     columns of the shared latent row).
+ *   page_table int32  [B][max_pages_per_req]; entry j of request b is the
+ *                     physical page holding tokens [j*P, (j+1)*P).
+ *   seqlens    int32  [B]; KV tokens of request b, the T new ones included.
+ *   out        bf16   [B][T][Hq][Dv]
+ *   lse        fp32   [B][T][Hq]; natural log of sum_j exp(scale * q.k_j).
+ *
+ * Semantics where the pages are silent
+ *   - query head h reads kv head h / (Hq/Hkv);
+ *   - the T query tokens are the last T cache positions; with `causal` query
+ *     token t sees keys j <= L - T + t;
+ *   - L == 0 gives out = 0 and lse = -inf;
+ *   - causal with 0 < L < T is an input error.
+ */
+#ifndef SKDECODE_H_
+#define SKDECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKD_ABI_VERSION 1
+/* KV tokens per planning granule; split points fall on multiples of it. */
+#define SKD_GRANULE 16
+
+typedef enum skd_status {
+  SKD_OK = 0,
+  SKD_EINVAL = 1,        /* bad argument: null pointer, negative size, misaligned pointer */
+  SKD_EUNSUPPORTED = 2,  /* valid but not implemented (head dims, page size, group size) */
+  SKD_ECUDA = 3,         /* a CUDA runtime or driver call failed */
+  SKD_EPLAN = 4,         /* plan buffer too small or inconsistent with the call */
+  SKD_ESIZE = 5          /* workspace too small */
+} skd_status;
+
+typedef enum skd_kind { SKD_KIND_GQA = 0, SKD_KIND_MLA = 1 } skd_kind;
+
+typedef enum skd_plan_mode {
+  SKD_PLAN_STREAMK = 0,      /* one-wave near-equal split (the method) */
+  SKD_PLAN_ROUND_ROBIN = 1   /* whole (request, kv head) items dealt in turn; comparator */
+} skd_plan_mode;
+
+/* Bits of the device error word (see skd_read_error). */
+#define SKD_DEVERR_PLAN 0x1      /* plan header does not match the launch */
+#define SKD_DEVERR_SEQLEN 0x2    /* a seqlen disagrees with the plan or the page table size */
+#define SKD_DEVERR_PAGE 0x4      /* a page id outside [0, num_pages) */
+#define SKD_DEVERR_TIMEOUT 0x8   /* a bounded wait inside the kernel gave up */
+
+typedef struct skd_shape {
+  int32_t batch;             /* B >= 0 */
+  int32_t q_tokens;          /* T >= 1 */
+  int32_t num_q_heads;       /* Hq */
+  int32_t num_kv_heads;      /* Hkv, divides Hq */
+  int32_t head_dim_qk;       /* Dk: GQA 64 or 128; MLA 576 */
+  int32_t head_dim_v;        /* Dv: GQA == Dk; MLA 512 */
+  int32_t page_size;         /* P, a multiple of SKD_GRANULE */
+  int32_t max_pages_per_req; /* columns of page_table */
+  int32_t num_pages;         /* NP, pages in k_pages (and v_pages) */
+  int32_t v_row_stride;      /* elements between consecutive V rows (>= Dv) */
+  float scale;               /* softmax scale applied to q.k (required) */
+  int32_t causal;            /* 1: mask among the T new tokens */
+  int32_t kind;              /* skd_kind */
+} skd_shape_t;
+
+/* ABI version of the loaded library (SKD_ABI_VERSION). */
+int skd_abi_version(void);
+
+/* Static text for a status code. */
+const char *skd_status_string(int status);
+
+/* Number of SMs of CUDA device `device` (one persistent CTA per SM is the
+ * intended grid). */
+int skd_device_sm_count(int device, int *sm_count_out);
+
+/* ---- planner ----------------------------------------------------------- */
+
+/* Bytes of a plan for `batch` requests, `num_kv_heads` heads, `n_ctas` CTAs.
+ * Returns 0 for invalid arguments. The plan has a fixed size for fixed
+ * (batch, num_kv_heads, n_ctas), so it can live in a graph-captured buffer. */
+size_t skd_plan_bytes(int batch, int num_kv_heads, int n_ctas);
+
+/* Host planner (pure function, no CUDA call). Splits the KV-token work of the
+ * batch into `n_ctas` chunks (mode SKD_PLAN_STREAMK) and writes the per-CTA
+ * segment list to `plan_host` (plan_bytes >= skd_plan_bytes(...)); copy it to
+ * the device before skd_decode_attention. Work item i = b*Hkv + h has
+ * ceil(seqlens[b] / SKD_GRANULE) granules; chunk c is granules
+ * [floor(c*G/n), floor((c+1)*G/n)) of all items in order, cut at item
+ * boundaries. seqlens_host: host int32[batch]; page_size must be a multiple
+ * of SKD_GRANULE. Errors: SKD_EINVAL (null pointer, n_ctas <= 0, negative
+ * seqlen, page_size), SKD_EPLAN (buffer too small, more than 2^31-1 granules). */
+int skd_decode_plan(const int32_t *seqlens_host, int batch, int num_kv_heads, int page_size,
+                    int n_ctas, int mode, void *plan_host, size_t plan_bytes);
+
+/* Device planner: the same plan, byte for byte, computed on the GPU from device
+ * seqlens by one kernel enqueued on `stream` (no host synchronisation, so it
+ * can be captured in a CUDA graph together with skd_decode_attention).
+ * seqlens_dev: device int32[batch]; plan_dev: device buffer of plan_bytes.
+ * Only mode SKD_PLAN_STREAMK. Bad seqlens (negative) set SKD_DEVERR_SEQLEN in
+ * the plan header's error field, which skd_decode_attention propagates. */
+int skd_decode_plan_device(const int32_t *seqlens_dev, int batch, int num_kv_heads,
+                           int page_size, int n_ctas, void *plan_dev, size_t plan_bytes,
+                           void *stream);
+
+/* ---- workspace --------------------------------------------------------- */
+
+/* Bytes of the workspace skd_decode_attention needs for this shape and grid:
+ * an error word, one arrival counter per (request, kv head) and room for the
+ * partial softmax states (m, l, acc) of up to 2*n_ctas splits. 0 if invalid. */
+size_t skd_workspace_bytes(const skd_shape_t *shape, int n_ctas);
+
+/* Zero the error word and all counters (enqueued on `stream`). Needed once
+ * after allocation and after any call that set a device error; the kernel
+ * itself returns every counter to zero after each successful call. */
+int skd_workspace_reset(void *ws_dev, size_t ws_bytes, void *stream);
+
+/* ---- the hot path ------------------------------------------------------ */
+
+/* Decode attention for the whole batch in one kernel launch of `n_ctas`
+ * persistent CTAs (the plan's CTA count) on `stream`. All tensor pointers are
+ * device pointers in the layouts above and must be 16-byte aligned; the plan
+ * (device copy) must have been built for shape->batch, shape->num_kv_heads and
+ * n_ctas. Asynchronous: returns after the launch. Errors detected on the host:
+ * SKD_EINVAL, SKD_EUNSUPPORTED, SKD_ESIZE, SKD_ECUDA (launch failure).
+ * Errors detected on the device set bits of the workspace error word
+ * (SKD_DEVERR_*); out and lse are then unspecified. Supported now:
+ * kind GQA with Dk == Dv in {64, 128} and (Hq/Hkv)*T <= 16;
+ * kind MLA with Dk 576, Dv 512, Hq 128, Hkv 1, T 1. */
+int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_pages,
+                         const void *v_pages, const int32_t *page_table, const int32_t *seqlens,
+                         const void *plan_dev, int n_ctas, void *ws_dev, size_t ws_bytes,
+                         void *out, float *lse, void *stream);
+
+/* Copy the device error word to *err_out (synchronises `stream`). */
+int skd_read_error(const void *ws_dev, int32_t *err_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SKDECODE_H_ */

@@ -1,0 +1,150 @@
+"""Stream-K split-KV decode attention over a paged KV cache, for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libskdecode.so`` (``include/skdecode.h``).
+Every step of the hot path runs in the library's CUDA kernels; this module only
+checks dtypes/devices and passes raw pointers, sizes and the current stream.
+PyTorch is used for device memory and streams.
+
+    plan = skd.plan(seqlens_cpu, num_kv_heads, page_size)        # host planner
+    plan_dev = plan.cuda()                                         # or skd.plan_device(...)
+    ws = skd.workspace(q, k_pages, v_pages, n_ctas)                # zeroed once
+    out, lse = skd.decode_attention(q, k_pages, v_pages, page_table, seqlens_dev,
+                                    plan_dev, ws, scale=..., causal=...)
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native as N
+from ._native import (SKD_DEVERR_PAGE, SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN,
+                      SKD_DEVERR_TIMEOUT, SKD_GRANULE, SkdError)
+
+__all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention", "read_error",
+           "sm_count", "make_shape", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
+           "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT"]
+
+_MODES = {"streamk": N.SKD_PLAN_STREAMK, "round_robin": N.SKD_PLAN_ROUND_ROBIN}
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> Optional[int]:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream or None
+
+
+def sm_count(device: Optional[int] = None) -> int:
+    dev = torch.cuda.current_device() if device is None else int(device)
+    v = ctypes.c_int(0)
+    N.check("skd_device_sm_count", N.lib().skd_device_sm_count(dev, ctypes.byref(v)))
+    return v.value
+
+
+def plan_bytes(batch: int, num_kv_heads: int, n_ctas: int) -> int:
+    return int(N.lib().skd_plan_bytes(batch, num_kv_heads, n_ctas))
+
+
+def plan(seqlens, num_kv_heads: int, page_size: int, n_ctas: Optional[int] = None,
+         mode: str = "streamk") -> torch.Tensor:
+    """Host planner. ``seqlens``: CPU int32 tensor (or anything torch.as_tensor
+    takes). Returns the plan as a CPU int32 tensor; copy it to the device."""
+    sl = torch.as_tensor(seqlens, dtype=torch.int32).contiguous()
+    if sl.device.type != "cpu":
+        raise ValueError("plan() takes host seqlens; use plan_device() for device seqlens")
+    n = sm_count() if n_ctas is None else int(n_ctas)
+    nb = plan_bytes(int(sl.numel()), num_kv_heads, n)
+    if nb == 0:
+        raise ValueError("invalid batch / num_kv_heads / n_ctas")
+    out = torch.zeros(nb // 4, dtype=torch.int32)
+    N.check("skd_decode_plan", N.lib().skd_decode_plan(
+        sl.data_ptr(), int(sl.numel()), int(num_kv_heads), int(page_size), n, _MODES[mode],
+        out.data_ptr(), nb))
+    return out
+
+
+def plan_device(seqlens: torch.Tensor, num_kv_heads: int, page_size: int, n_ctas: int,
+                out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Device planner (graph capturable). ``seqlens``: CUDA int32 tensor."""
+    if seqlens.device.type != "cuda" or seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
+        raise ValueError("seqlens must be a contiguous CUDA int32 tensor")
+    nb = plan_bytes(int(seqlens.numel()), num_kv_heads, n_ctas)
+    if out is None:
+        out = torch.empty(nb // 4, dtype=torch.int32, device=seqlens.device)
+    N.check("skd_decode_plan_device", N.lib().skd_decode_plan_device(
+        seqlens.data_ptr(), int(seqlens.numel()), int(num_kv_heads), int(page_size), int(n_ctas),
+        out.data_ptr(), out.numel() * 4, _stream_ptr(stream)))
+    return out
+
+
+def make_shape(q: torch.Tensor, k_pages: torch.Tensor, v_pages: Optional[torch.Tensor],
+               page_table: torch.Tensor, *, scale: float, causal: bool,
+               head_dim_v: Optional[int] = None) -> N.Shape:
+    """skd_shape_t from tensor shapes. GQA: q [B,T,Hq,D], k/v [NP,P,Hkv,D].
+    Absorbed MLA: v_pages None, k_pages [NP,P,576] or [NP,P,1,576], Dv 512."""
+    B, T, Hq, Dk = (int(x) for x in q.shape)
+    mla = v_pages is None
+    if mla:
+        NP, P = int(k_pages.shape[0]), int(k_pages.shape[1])
+        Hkv, Dv, vstride = 1, int(head_dim_v or 512), Dk
+    else:
+        NP, P, Hkv = (int(x) for x in k_pages.shape[:3])
+        Dv = int(v_pages.shape[3])
+        vstride = Dv
+    return N.Shape(batch=B, q_tokens=T, num_q_heads=Hq, num_kv_heads=Hkv, head_dim_qk=Dk,
+                   head_dim_v=Dv, page_size=P, max_pages_per_req=int(page_table.shape[1]),
+                   num_pages=NP, v_row_stride=vstride, scale=float(scale), causal=int(bool(causal)),
+                   kind=N.SKD_KIND_MLA if mla else N.SKD_KIND_GQA)
+
+
+def workspace(shape: N.Shape, n_ctas: int, device=None) -> torch.Tensor:
+    """Allocate and zero the workspace for ``shape`` and ``n_ctas`` CTAs."""
+    nb = int(N.lib().skd_workspace_bytes(ctypes.byref(shape), int(n_ctas)))
+    if nb == 0:
+        raise SkdError("skd_workspace_bytes", N.SKD_EUNSUPPORTED)
+    ws = torch.empty(nb, dtype=torch.uint8, device=device or "cuda")
+    N.check("skd_workspace_reset", N.lib().skd_workspace_reset(ws.data_ptr(), nb, _stream_ptr(None)))
+    return ws
+
+
+def _chk(t: torch.Tensor, name: str, dtype):
+    if t.device.type != "cuda" or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def decode_attention(q, k_pages, v_pages, page_table, seqlens, plan_dev, ws, *, scale: float,
+                     causal: Optional[bool] = None, n_ctas: Optional[int] = None,
+                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                     shape: Optional[N.Shape] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Enqueue one decode-attention launch; returns (out bf16 [B,T,Hq,Dv], lse fp32 [B,T,Hq])."""
+    _chk(q, "q", torch.bfloat16)
+    _chk(k_pages, "k_pages", torch.bfloat16)
+    if v_pages is not None:
+        _chk(v_pages, "v_pages", torch.bfloat16)
+    _chk(page_table, "page_table", torch.int32)
+    _chk(seqlens, "seqlens", torch.int32)
+    _chk(plan_dev, "plan", torch.int32)
+    if causal is None:
+        causal = q.shape[1] > 1
+    if shape is None:
+        shape = make_shape(q, k_pages, v_pages, page_table, scale=scale, causal=causal)
+    B, T, Hq = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    if out is None:
+        out = torch.empty(B, T, Hq, shape.head_dim_v, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, Hq, dtype=torch.float32, device=q.device)
+    n = int(plan_dev[3].item()) if n_ctas is None else int(n_ctas)
+    vp = k_pages if v_pages is None else v_pages
+    N.check("skd_decode_attention", N.lib().skd_decode_attention(
+        ctypes.byref(shape), q.data_ptr(), k_pages.data_ptr(), vp.data_ptr(), page_table.data_ptr(),
+        seqlens.data_ptr(), plan_dev.data_ptr(), n, ws.data_ptr(), ws.numel(), out.data_ptr(),
+        lse.data_ptr(), _stream_ptr(stream)))
+    return out, lse
+
+
+def read_error(ws: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    v = ctypes.c_int32(0)
+    N.check("skd_read_error", N.lib().skd_read_error(ws.data_ptr(), ctypes.byref(v), _stream_ptr(stream)))
+    return int(v.value)

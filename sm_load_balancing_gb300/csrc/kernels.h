@@ -1,0 +1,45 @@
+// Internal launcher interface between the C-ABI layer and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "skdecode.h"
+
+namespace skd {
+
+// Workspace layout: [0,256) error word; counters (one int32 per item);
+// partial-state slots (2 per CTA), each holding O[rows][Dv], m[rows], l[rows]
+// in fp32 (m in log2 units of the scaled score).
+struct WsLayout {
+  int64_t counters, partials, slot_floats, slots, bytes;
+  int rows;
+};
+WsLayout ws_layout(const skd_shape_t &s, int n_ctas);
+
+struct DecodeArgs {
+  skd_shape_t shape;
+  const void *q, *k, *v;
+  const int32_t *page_table, *seqlens, *plan;
+  int n_ctas;
+  void *ws;
+  WsLayout wl;
+  void *out;
+  float *lse;
+  cudaStream_t stream;
+};
+
+int launch_gqa(const DecodeArgs &a);
+int launch_mla(const DecodeArgs &a);
+int launch_plan_device(const int32_t *seqlens, int batch, int hkv, int n_ctas, int32_t *plan,
+                       cudaStream_t stream);
+
+// cuTensorMapEncodeTiled, looked up through the runtime (no libcuda link).
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, cuuint32_t rank, void *gaddr,
+                      const cuuint64_t *gdim, const cuuint64_t *gstride, const cuuint32_t *box,
+                      const cuuint32_t *estride, CUtensorMapSwizzle swz);
+
+// Bounded device waits give up after this many SM cycles (about one second).
+constexpr long long kWaitCycles = 2000000000LL;
+
+}  // namespace skd

@@ -1,0 +1,135 @@
+// Host planner: the Stream-K one-wave split of a decode batch.
+//
+// "传统 GEMM 计算可能因任务大小不均产生多个调度波次（Waves）..." (triton.csdn.net Q&A
+// on waves and FlashMLA's Stream-K), closing summary: cut the total work into
+// exactly as many near-equal chunks as there are SMs and launch one wave, so no
+// tail wave waits on a slow CTA. "MeldKernel：动态负载下跨 SM 融合内核（SOSP 2026）",
+// core method: the mapping is decided at run time from the actual lengths.
+//
+// Work item i = b*Hkv + h carries ceil(L_b / 16) granules; CTA c receives the
+// granule range [floor(c*G/n), floor((c+1)*G/n)) of the items laid end to end,
+// cut at item boundaries. A single linear sweep, O(items + n).
+#include <string.h>
+
+#include <vector>
+
+#include "plan_layout.h"
+#include "skdecode.h"
+
+namespace skd {
+
+static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int build_plan_host(const int32_t *seqlens, int batch, int hkv, int page_size, int n, int mode,
+                    void *plan_out, size_t plan_bytes) {
+  if (!seqlens && batch > 0) return SKD_EINVAL;
+  if (!plan_out || batch < 0 || hkv <= 0 || n <= 0) return SKD_EINVAL;
+  if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
+  if (mode != SKD_PLAN_STREAMK && mode != SKD_PLAN_ROUND_ROBIN) return SKD_EINVAL;
+  const PlanOffsets off = plan_offsets(batch, hkv, n);
+  if (plan_bytes < size_t(off.words) * 4) return SKD_EPLAN;
+  for (int b = 0; b < batch; ++b)
+    if (seqlens[b] < 0) return SKD_EINVAL;
+
+  const int64_t items = int64_t(batch) * hkv;
+  const int64_t cap = items + n;
+  int32_t *w = static_cast<int32_t *>(plan_out);
+  memset(w, 0, size_t(off.words) * 4);
+  int32_t *cta_off = w + off.cta_off;
+  int32_t *segs = w + off.segs;
+  int32_t *nsplit = w + off.nsplit;
+  int32_t *slot0 = w + off.slot0;
+
+  int64_t total = 0;
+  for (int b = 0; b < batch; ++b) total += int64_t(hkv) * ceil_div(seqlens[b], kGranule);
+  if (total > INT32_MAX) return SKD_EPLAN;
+
+  int64_t nseg = 0;
+  auto push = [&](int64_t item, int64_t tb, int64_t te) {
+    int32_t *s = segs + 4 * nseg;
+    s[0] = int32_t(item);
+    s[1] = int32_t(tb);
+    s[2] = int32_t(te);
+    s[3] = -1;
+    ++nseg;
+  };
+
+  if (mode == SKD_PLAN_STREAMK) {
+    auto bound = [&](int64_t c) { return (c * total) / n; };
+    int64_t c = 0, pos = 0;
+    cta_off[0] = 0;
+    auto close_ctas_up_to = [&](int64_t cnew) {
+      // CTAs c .. cnew-1 are complete: record where CTA c+1.. begins
+      while (c < cnew) {
+        ++c;
+        cta_off[c] = int32_t(nseg);
+      }
+    };
+    for (int64_t i = 0; i < items; ++i) {
+      const int64_t L = seqlens[i / hkv];
+      const int64_t g = ceil_div(L, kGranule);
+      const int64_t s = pos, e = pos + g;
+      pos = e;
+      // first CTA whose chunk ends after s (the last CTA if none)
+      int64_t cs = c;
+      while (cs < n - 1 && bound(cs + 1) <= s) ++cs;
+      close_ctas_up_to(cs);
+      if (g == 0) {
+        push(i, 0, 0);
+        continue;
+      }
+      for (int64_t cc = cs; cc < n; ++cc) {
+        const int64_t lo = s > bound(cc) ? s : bound(cc);
+        const int64_t hi = e < bound(cc + 1) ? e : bound(cc + 1);
+        if (lo >= hi) {
+          if (bound(cc) >= e) break;
+          continue;
+        }
+        close_ctas_up_to(cc);
+        const int64_t tb = (lo - s) * kGranule;
+        const int64_t te = (hi - s) * kGranule < L ? (hi - s) * kGranule : L;
+        push(i, tb, te);
+      }
+    }
+    close_ctas_up_to(n);
+    cta_off[n] = int32_t(nseg);
+  } else {
+    // round robin: item i -> CTA i mod n, no splits
+    for (int64_t c = 0; c < n; ++c) {
+      cta_off[c] = int32_t(nseg);
+      for (int64_t i = c; i < items; i += n) push(i, 0, seqlens[i / hkv]);
+    }
+    cta_off[n] = int32_t(nseg);
+  }
+  if (nseg > cap) return SKD_EPLAN;  // cannot happen by construction
+
+  // splits per item (segments of an item are consecutive in the list)
+  int64_t nslots = 0;
+  for (int64_t k = 0; k < nseg;) {
+    const int32_t item = segs[4 * k];
+    int64_t e = k;
+    while (e < nseg && segs[4 * e] == item) ++e;
+    const int64_t ns = e - k;
+    nsplit[item] = int32_t(ns);
+    slot0[item] = ns > 1 ? int32_t(nslots) : -1;
+    if (ns > 1)
+      for (int64_t j = k; j < e; ++j) segs[4 * j + 3] = int32_t(nslots++);
+    k = e;
+  }
+
+  w[PH_MAGIC] = kPlanMagic;
+  w[PH_BATCH] = batch;
+  w[PH_HKV] = hkv;
+  w[PH_NCTAS] = n;
+  w[PH_GRANULE] = kGranule;
+  w[PH_NITEMS] = int32_t(items);
+  w[PH_NSEGS] = int32_t(nseg);
+  w[PH_NSLOTS] = int32_t(nslots);
+  w[PH_TOTAL] = int32_t(total);
+  w[PH_MODE] = mode;
+  w[PH_SEGCAP] = int32_t(cap);
+  w[PH_ERR] = 0;
+  return SKD_OK;
+}
+
+}  // namespace skd

@@ -1,0 +1,172 @@
+"""Host-side checks of libskdecode.so (no GPU needed): every symbol the header
+declares is exported, the host planner equals the Stream-K definition in the
+oracle bit for bit, and argument validation rejects bad calls before any CUDA
+work is enqueued."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import streamk as S
+from tests import plan_decode as PD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def N():
+    from sm_load_balancing_gb300 import build as B
+    B.build()
+    from sm_load_balancing_gb300 import _native
+    _native.lib()
+    return _native
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(skd_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(N):
+    lib = N.lib()
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert declared == set(N.SIGNATURES), declared ^ set(N.SIGNATURES)
+    assert lib.skd_abi_version() == 1
+
+
+def _host_plan(N, seqlens, hkv, n, mode=0, page_size=16):
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    nb = N.lib().skd_plan_bytes(len(sl), hkv, n)
+    buf = np.zeros(nb // 4, dtype=np.int32)
+    st = N.lib().skd_decode_plan(sl.ctypes.data, len(sl), hkv, page_size, n, mode, buf.ctypes.data, nb)
+    return st, buf
+
+
+def _check_against_oracle(N, seqlens, hkv, n):
+    st, buf = _host_plan(N, seqlens, hkv, n)
+    assert st == 0
+    p = PD.decode(buf)
+    ref = S.streamk_split(seqlens, hkv, n, granule=16)
+    got = [[(i, tb, te) for i, tb, te, _ in segs] for segs in p["segments"]]
+    assert got == ref["segments"]
+    assert p["total"] == ref["total_granules"]
+    # slots: items with k > 1 splits own k consecutive slots, numbered in item order
+    nxt = 0
+    for i, splits in enumerate(ref["item_splits"]):
+        assert p["nsplit"][i] == len(splits)
+        if len(splits) > 1:
+            assert p["slot0"][i] == nxt
+            nxt += len(splits)
+        else:
+            assert p["slot0"][i] == -1
+    assert p["nslots"] == nxt <= 2 * n
+    for segs in p["segments"]:
+        for i, tb, te, slot in segs:
+            if p["nsplit"][i] == 1:
+                assert slot == -1
+            else:
+                k = [x[1] for x in ref["item_splits"][i]].index(tb)
+                assert slot == p["slot0"][i] + k
+    assert p["nseg"] <= p["cap"]
+    return p
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_host_planner_equals_streamk_definition(N, seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(0, 9))
+    hkv = int(rng.integers(1, 5))
+    n = int(rng.choice([1, 2, 3, 7, 13, 148, 152, 304]))
+    seqlens = [int(x) for x in rng.integers(0, 400, size=B)]
+    if B and seed % 3 == 0:
+        seqlens[int(rng.integers(0, B))] = 0
+    _check_against_oracle(N, seqlens, hkv, n)
+
+
+@pytest.mark.parametrize("name", ["tiny_gqa", "llama3_8b_gqa", "skewed_gqa", "mla_absorbed",
+                                  "speculative_gqa"])
+@pytest.mark.parametrize("n", [148, 152])
+def test_host_planner_on_named_workloads(N, name, n):
+    sl = W.draw_seqlens(name)
+    hkv = {"tiny_gqa": 2, "mla_absorbed": 1}.get(name, 8)
+    p = _check_against_oracle(N, sl.tolist(), hkv, n)
+    per = [sum(-(-(te - tb) // 16) for _, tb, te, _ in segs) for segs in p["segments"]]
+    assert max(per) - min(per) <= 1
+
+
+def test_round_robin_mode_matches_definition(N):
+    seqlens = [5, 0, 9, 100, 33]
+    st, buf = _host_plan(N, seqlens, 2, 4, mode=1)
+    assert st == 0
+    p = PD.decode(buf)
+    ref = S.round_robin_split(seqlens, 2, 4)
+    assert [[s[:3] for s in segs] for segs in p["segments"]] == ref["segments"]
+    assert p["nslots"] == 0 and all(ns == 1 for ns in p["nsplit"])
+
+
+def test_planner_errors(N):
+    st, _ = _host_plan(N, [10, -1], 1, 4)
+    assert st == N.SKD_EINVAL
+    st, _ = _host_plan(N, [10, 20], 1, 4, page_size=8)
+    assert st == N.SKD_EINVAL
+    sl = np.array([10, 20], np.int32)
+    buf = np.zeros(4, np.int32)
+    assert N.lib().skd_decode_plan(sl.ctypes.data, 2, 1, 16, 4, 0, buf.ctypes.data, 16) == N.SKD_EPLAN
+    assert N.lib().skd_plan_bytes(2, 0, 4) == 0
+
+
+def _shape(N, **kw):
+    d = dict(batch=2, q_tokens=1, num_q_heads=8, num_kv_heads=2, head_dim_qk=64, head_dim_v=64,
+             page_size=16, max_pages_per_req=16, num_pages=16, v_row_stride=64, scale=0.125,
+             causal=0, kind=0)
+    d.update(kw)
+    return N.Shape(**d)
+
+
+def test_workspace_bytes(N):
+    lib = N.lib()
+    s = _shape(N)
+    nb = lib.skd_workspace_bytes(ctypes.byref(s), 148)
+    rows = 4
+    slot = -(-rows * 66 // 4) * 4
+    assert nb == 256 + 256 + 2 * 148 * slot * 4  # counters fit in the first 256-byte block
+    assert lib.skd_workspace_bytes(ctypes.byref(_shape(N, head_dim_qk=96, head_dim_v=96,
+                                                       v_row_stride=96)), 148) == 0
+    assert lib.skd_workspace_bytes(ctypes.byref(_shape(N, num_q_heads=64, num_kv_heads=2)), 8) == 0
+    mla = _shape(N, num_q_heads=128, num_kv_heads=1, head_dim_qk=576, head_dim_v=512,
+                 v_row_stride=576, kind=1, page_size=64)
+    assert lib.skd_workspace_bytes(ctypes.byref(mla), 148) > 0
+
+
+def test_decode_attention_rejects_bad_arguments_before_launch(N):
+    lib = N.lib()
+    fake = 1 << 20  # never dereferenced: validation fails first
+    s = _shape(N)
+
+    def call(shape, q=fake, ws_bytes=1 << 30, n=4, ws=fake):
+        return lib.skd_decode_attention(ctypes.byref(shape), q, fake, fake, fake, fake, fake, n,
+                                        ws, ws_bytes, fake, fake, None)
+
+    assert call(s, q=fake + 2) == N.SKD_EINVAL                      # misaligned q
+    assert call(s, q=0) == N.SKD_EINVAL                             # null
+    assert call(s, n=0) == N.SKD_EINVAL
+    assert call(s, ws_bytes=100) == N.SKD_ESIZE
+    assert call(_shape(N, head_dim_qk=80, head_dim_v=80, v_row_stride=80)) == N.SKD_EUNSUPPORTED
+    assert call(_shape(N, page_size=8)) == N.SKD_EUNSUPPORTED
+    assert call(_shape(N, num_q_heads=7)) == N.SKD_EINVAL
+    assert call(_shape(N, scale=float("nan"))) == N.SKD_EINVAL
+    assert call(_shape(N, kind=5)) == N.SKD_EINVAL
+    assert call(_shape(N, batch=0)) == N.SKD_OK                     # nothing to do
+    assert lib.skd_status_string(N.SKD_ESIZE) == b"workspace too small"

@@ -46,11 +46,23 @@ def bf16_bits_to_fp32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal_bf16(rng: np.random.Generator, n: int, chunk: int = 1 << 25) -> np.ndarray:
+def _normal_bf16(rng: np.random.Generator, n: int, chunk: int = 1 << 20) -> np.ndarray:
+    """n fp32 N(0,1) draws rounded to bf16 (same values as fp32_to_bf16_bits of
+    one big draw; chunked only to avoid large temporaries)."""
     out = np.empty(n, dtype=np.uint16)
+    buf = np.empty(chunk, dtype=np.float32)
+    u = buf.view(np.uint32)
+    tmp = np.empty(chunk, dtype=np.uint32)
     for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        out[s:e] = fp32_to_bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+        m = min(n, s + chunk) - s
+        rng.standard_normal(out=buf[:m], dtype=np.float32)
+        t = tmp[:m]
+        np.right_shift(u[:m], 16, out=t)
+        np.bitwise_and(t, 1, out=t)
+        np.add(t, 0x7FFF, out=t)
+        np.add(u[:m], t, out=t)
+        np.right_shift(t, 16, out=t)
+        out[s:s + m] = t
     return out
 
 
