@@ -48,8 +48,9 @@ struct Smem {
   static constexpr int kQOff = kStages * kStageBytes;
   static constexpr int kOOff = kQOff + 2 * kQBytes;
   static constexpr int kMOff = kOOff + kCWarps * 16 * kOStride * 4;
-  static constexpr int kLOff = kMOff + kCWarps * 16 * 4;
-  static constexpr int kBarOff = kLOff + kCWarps * 16 * 4;
+  static constexpr int kLOff = kMOff + kCWarps * 16 * 4;   // sum of bf16-rounded p
+  static constexpr int kLfOff = kLOff + kCWarps * 16 * 4;  // sum of fp32 p
+  static constexpr int kBarOff = kLfOff + kCWarps * 16 * 4;
   static constexpr int kNumBars = 2 * kStages + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *sm_o = reinterpret_cast<float *>(smem + S::kOOff);
   float *sm_m = reinterpret_cast<float *>(smem + S::kMOff);
   float *sm_l = reinterpret_cast<float *>(smem + S::kLOff);
+  float *sm_lf = reinterpret_cast<float *>(smem + S::kLfOff);
   const float NEG_INF = -INFINITY;
   int stage = 0, qs = 0;
   uint32_t phase = 0, qph = 0;
@@ -266,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float o[D / 8][4];
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+    // l: sum of the bf16-rounded p that enter P.V (normalises out, so out is an
+    // exact convex combination of V rows); lf: sum of fp32 p (gives lse)
+    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f, lf0 = 0.f, lf1 = 0.f;
 
     for (int tok0 = tb; tok0 < te; tok0 += kBlockN) {
       if (alive && !ptx::mbar_wait(full_bar(stage), phase, abort_flag, kWaitCycles)) {
@@ -332,11 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         m0 = mn0;
         m1 = mn1;
         uint32_t pa[4];
-        float ps0 = 0.f, ps1 = 0.f;
+        float ps0 = 0.f, ps1 = 0.f, pf0 = 0.f, pf1 = 0.f;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const uint32_t u0 = ptx::pack_bf16(exp2f(s[j][0] - mu0), exp2f(s[j][1] - mu0));
-          const uint32_t u1 = ptx::pack_bf16(exp2f(s[j][2] - mu1), exp2f(s[j][3] - mu1));
+          const float e00 = exp2f(s[j][0] - mu0), e01 = exp2f(s[j][1] - mu0);
+          const float e10 = exp2f(s[j][2] - mu1), e11 = exp2f(s[j][3] - mu1);
+          pf0 += e00 + e01;
+          pf1 += e10 + e11;
+          const uint32_t u0 = ptx::pack_bf16(e00, e01);
+          const uint32_t u1 = ptx::pack_bf16(e10, e11);
           const float2 f0 = ptx::unpack_bf16(u0), f1 = ptx::unpack_bf16(u1);
           ps0 += f0.x + f0.y;
           ps1 += f1.x + f1.y;
@@ -345,6 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l0 = l0 * a0 + ps0;
         l1 = l1 * a1 + ps1;
+        lf0 = lf0 * a0 + pf0;
+        lf1 = lf1 * a1 + pf1;
 #pragma unroll
         for (int j = 0; j < D / 8; ++j) {
           o[j][0] *= a0;
@@ -381,11 +391,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    lf0 += __shfl_xor_sync(0xffffffffu, lf0, 1);
+    lf0 += __shfl_xor_sync(0xffffffffu, lf0, 2);
+    lf1 += __shfl_xor_sync(0xffffffffu, lf1, 1);
+    lf1 += __shfl_xor_sync(0xffffffffu, lf1, 2);
     if (fc == 0) {
       sm_m[w * 16 + r0] = m0;
       sm_m[w * 16 + r1] = m1;
       sm_l[w * 16 + r0] = l0;
       sm_l[w * 16 + r1] = l1;
+      sm_lf[w * 16 + r0] = lf0;
+      sm_lf[w * 16 + r1] = lf1;
     }
     {
       float *ow = sm_o + w * 16 * S::kOStride;
@@ -400,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool split = wslot >= 0;
     const bool live = !*abort_flag;
     float acc[D / 8];
-    float M = NEG_INF, Lt = 0.f;
+    float M = NEG_INF, Lt = 0.f, Lf = 0.f;
     if (cr < rows && live) {
 #pragma unroll
       for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, sm_m[ww * 16 + cr]);
@@ -411,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ww = 0; ww < kCWarps; ++ww) {
         const float f = exp2f(sm_m[ww * 16 + cr] - Mu);
         Lt += sm_l[ww * 16 + cr] * f;
+        Lf += sm_lf[ww * 16 + cr] * f;
         const float *src = sm_o + (ww * 16 + cr) * S::kOStride + cb;
 #pragma unroll
         for (int c = 0; c < D / 8; c += 4) {
@@ -429,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int4 *o4 = reinterpret_cast<int4 *>(p.out + orow * D + cb);
 #pragma unroll
         for (int i = 0; i < D / 64; ++i) o4[i] = make_int4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        if ((tid & 7) == 0) p.lse[orow] = (M + log2f(Lt)) * 0.69314718055994531f;
+        if ((tid & 7) == 0) p.lse[orow] = (M + log2f(Lf)) * 0.69314718055994531f;
       } else {
         float *ps = p.partials + int64_t(wslot) * p.slot_floats;
         float4 *d4 = reinterpret_cast<float4 *>(ps + cr * D + cb);
@@ -438,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((tid & 7) == 0) {
           ps[rows * D + cr] = M;
           ps[rows * D + rows + cr] = Lt;
+          ps[rows * D + 2 * rows + cr] = Lf;
         }
       }
     }
@@ -464,13 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < nsp; ++s)
             Mx = fmaxf(Mx, __ldcg(p.partials + int64_t(s0 + s) * p.slot_floats + rows * D + cr));
           const float Mu = Mx == NEG_INF ? 0.f : Mx;
-          float lam = 0.f;
+          float lam = 0.f, lamf = 0.f;
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
           for (int s = 0; s < nsp; ++s) {
             const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats;
             const float f = exp2f(__ldcg(ps + rows * D + cr) - Mu);
             lam += __ldcg(ps + rows * D + rows + cr) * f;
+            lamf += __ldcg(ps + rows * D + 2 * rows + cr) * f;
             const float4 *src = reinterpret_cast<const float4 *>(ps + cr * D + cb);
 #pragma unroll
             for (int c = 0; c < D / 8; c += 4) {
@@ -489,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < D / 64; ++i)
             o4[i] = make_int4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          if ((tid & 7) == 0) p.lse[orow] = (Mx + log2f(lam)) * 0.69314718055994531f;
+          if ((tid & 7) == 0) p.lse[orow] = (Mx + log2f(lamf)) * 0.69314718055994531f;
         }
         if (tid == 0) p.counters[item] = 0;
       }

@@ -9,8 +9,9 @@
 namespace skd {
 
 // Workspace layout: [0,256) error word; counters (one int32 per item);
-// partial-state slots (2 per CTA), each holding O[rows][Dv], m[rows], l[rows]
-// in fp32 (m in log2 units of the scaled score).
+// partial-state slots (2 per CTA), each holding O[rows][Dv], m[rows], l[rows],
+// lf[rows] in fp32 (m in log2 units of the scaled score; l sums the bf16-rounded
+// probabilities that entered P.V, lf the fp32 ones).
 struct WsLayout {
   int64_t counters, partials, slot_floats, slots, bytes;
   int rows;

@@ -53,7 +53,7 @@ WsLayout ws_layout(const skd_shape_t &s, int n_ctas) {
   w.rows = item_rows(s);
   w.counters = 256;
   w.partials = align_up(w.counters + 4 * items, 256);
-  w.slot_floats = align_up(int64_t(w.rows) * (s.head_dim_v + 2), 4);
+  w.slot_floats = align_up(int64_t(w.rows) * (s.head_dim_v + 3), 4);
   w.slots = 2 * int64_t(n_ctas);
   w.bytes = w.partials + w.slots * w.slot_floats * 4;
   return w;

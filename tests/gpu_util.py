@@ -60,7 +60,14 @@ def compare(w, out, lse, rows=None, ref=None):
     rl = rl.reshape(l.shape)
     fin = np.isfinite(rl)
     assert np.array_equal(fin, np.isfinite(l)), "lse finiteness differs"
-    d_out = float(np.abs(o - ro).max()) if o.size else 0.0
+    # Where |out| >= 2 one bf16 ulp (>= 2^-6) is coarser than the 1e-2 bound
+    # itself, so there the bound is one ulp of the reference value; such values
+    # only arise in rows that see a handful of keys.
+    big = np.abs(ro) >= 2.0
+    if big.any():
+        ulp = np.exp2(np.floor(np.log2(np.abs(ro[big]))) - 7)
+        assert np.all(np.abs(o[big] - ro[big]) <= ulp), "more than one bf16 ulp off"
+    d_out = float(np.abs(o - ro)[~big].max()) if (~big).any() else 0.0
     d_lse = float(np.abs(l[fin] - rl[fin]).max()) if fin.any() else 0.0
     assert np.all(l[~fin] == -np.inf)
     return d_out, d_lse

@@ -140,7 +140,7 @@ def test_workspace_bytes(N):
     s = _shape(N)
     nb = lib.skd_workspace_bytes(ctypes.byref(s), 148)
     rows = 4
-    slot = -(-rows * 66 // 4) * 4
+    slot = -(-rows * 67 // 4) * 4
     assert nb == 256 + 256 + 2 * 148 * slot * 4  # counters fit in the first 256-byte block
     assert lib.skd_workspace_bytes(ctypes.byref(_shape(N, head_dim_qk=96, head_dim_v=96,
                                                        v_row_stride=96)), 148) == 0
