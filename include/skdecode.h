@@ -120,9 +120,12 @@ size_t skd_plan_bytes(int batch, int num_kv_heads, int n_ctas);
 /* Host planner (pure function, no CUDA call). Splits the KV-token work of the
  * batch into `n_ctas` chunks (mode SKD_PLAN_STREAMK) and writes the per-CTA
  * segment list to `plan_host` (plan_bytes >= skd_plan_bytes(...)); copy it to
- * the device before skd_decode_attention. Work item i = b*Hkv + h has
- * ceil(seqlens[b] / SKD_GRANULE) granules; chunk c is granules
- * [floor(c*G/n), floor((c+1)*G/n)) of all items in order, cut at item
+ * the device before skd_decode_attention.
+ * The kv heads of a request are processed in groups of HG heads, HG = the
+ * largest divisor of num_kv_heads not above 8 (so NGRP = num_kv_heads / HG
+ * groups; MLA: 1). Work item i = b*NGRP + g has ceil(seqlens[b] / SKD_GRANULE)
+ * granules (a granule = SKD_GRANULE tokens of all HG heads); chunk c is
+ * granules [floor(c*G/n), floor((c+1)*G/n)) of all items in order, cut at item
  * boundaries. seqlens_host: host int32[batch]; page_size must be a multiple
  * of SKD_GRANULE. Errors: SKD_EINVAL (null pointer, n_ctas <= 0, negative
  * seqlen, page_size), SKD_EPLAN (buffer too small, more than 2^31-1 granules). */
@@ -142,8 +145,9 @@ int skd_decode_plan_device(const int32_t *seqlens_dev, int batch, int num_kv_hea
 /* ---- workspace --------------------------------------------------------- */
 
 /* Bytes of the workspace skd_decode_attention needs for this shape and grid:
- * an error word, one arrival counter per (request, kv head) and room for the
- * partial softmax states (m, l, acc) of up to 2*n_ctas splits. 0 if invalid. */
+ * an error word, one arrival counter per work item (request, kv-head group),
+ * one merge-tree counter per split slot and room for the partial softmax
+ * states (m, l, acc) of up to 2*n_ctas splits. 0 if invalid. */
 size_t skd_workspace_bytes(const skd_shape_t *shape, int n_ctas);
 
 /* Zero the error word and all counters (enqueued on `stream`). Needed once
@@ -170,6 +174,22 @@ int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_
 
 /* Copy the device error word to *err_out (synchronises `stream`). */
 int skd_read_error(const void *ws_dev, int32_t *err_out, void *stream);
+
+/* ---- diagnostics ------------------------------------------------------- */
+
+/* Per-CTA execution trace, after the GLM-5.2 decode article's Kineto analysis
+ * of how busy the SMs are (duration-weighted SM busy fraction, idle bubbles).
+ * While enabled (trace_dev != NULL) every decode-attention launch adds, for CTA
+ * c, SKD_TRACE_RECORD_BYTES at trace_dev + c*SKD_TRACE_RECORD_BYTES: int64
+ * words {0: %globaltimer ns at start, 1: ns at end, 2: consumer cycles spent
+ * waiting for data (summed over consumer warps), 3: consumer cycles in total
+ * (summed), 4: producer cycles waiting for free stages, 5: producer cycles in
+ * total, 6: segments, 7: pipeline stages}. Words 2, 3 and 7 are accumulated
+ * with atomics: zero the buffer before each launch. A buffer smaller than
+ * n_ctas records disables tracing for that launch. Process-wide setting, not
+ * thread-safe; pass NULL to disable. Errors: SKD_EINVAL (misaligned pointer). */
+#define SKD_TRACE_RECORD_BYTES 64
+int skd_trace_enable(void *trace_dev, size_t bytes);
 
 #ifdef __cplusplus
 }

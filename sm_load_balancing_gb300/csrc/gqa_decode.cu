@@ -2,27 +2,36 @@
 //
 // One persistent wave: CTA c walks the segment list the planner gave it (a
 // near-equal share of the batch's KV tokens; triton.csdn.net Q&A on waves and
-// FlashMLA's Stream-K, closing summary). Per segment (request b, kv head h,
-// token range) the CTA streams paged K/V with TMA and keeps an online softmax
-// ("GPU Kernel、异步 Launch、Stream 与融合 Kernel 全解", section 6.3 / Q8:
-// QK^T -> mask -> softmax -> xV without writing scores to HBM). A segment that
-// is only part of its (b, h) item writes its partial state (m, l, acc) to an
-// L2-resident workspace slot and bumps the item's arrival counter; the split
-// that arrives last merges all partials of the item right there
+// FlashMLA's Stream-K, closing summary). Per segment (request b, kv-head group
+// g, token range) the CTA streams paged K/V with TMA and keeps an online
+// softmax per query row ("GPU Kernel、异步 Launch、Stream 与融合 Kernel 全解",
+// section 6.3 / Q8: QK^T -> mask -> softmax -> xV without writing scores to
+// HBM). A segment that is only part of its (b, g) item writes its partial
+// state (m, l, acc) to an L2-resident workspace slot and counts its arrival;
+// the split that arrives last merges the partials right there
 // ("MeldKernel：动态负载下跨 SM 融合内核（SOSP 2026）", core method:
 // just-in-time reduction, no separate reduction kernel and no wait for the
-// slowest split). Nobody ever waits for another CTA, so the kernel is correct
-// for any grid size and any scheduling order.
+// slowest split). Items with more than 8 splits merge as a two-level tree:
+// the last arriver of each run of 8 consecutive splits folds them into one
+// partial, and the last of those runs folds the runs. Nobody waits for
+// another CTA, so the kernel is correct for any grid size and any scheduling
+// order.
 //
-// CTA layout: warps 0..3 consume, warp 4 (one lane) produces.
-//   stage  = 64 tokens of one kv head: K and V tiles, each D/64 sub-tiles of
-//            [64 rows][128 B] with the 128-byte TMA swizzle;
-//   warp w = the w-th 16-token granule of every stage; it keeps its own
-//            (m, l, O) for the rows of the item and the four warps are merged
-//            in shared memory at the end of the segment.
-//   rows   = the G*T query rows sharing kv head h (padded to 16 for
-//            mma.sync m16n8k16; row r is query token r / G, head h*G + r % G).
+// CTA layout: warps 0..HG-1 consume (warp h = kv head g*HG + h of the group),
+// warp HG (lane 0) produces.
+//   stage = one 16-token granule of all HG heads: K and V tiles, each loaded
+//           by ONE TMA box of the 5-D map {64 dims, tokens, D/64 halves,
+//           heads, pages} (dims listed out of stride order so that the tile
+//           lands as [head][half][16 tokens][128 B], 128-byte swizzle: the
+//           eight rows an ldmatrix reads are eight different tokens, so the
+//           swizzle spreads them over all banks). 32 KB per box for 8 heads
+//           of 128 dims: measured on GB300, boxes this large stream at
+//           ~7.2 TB/s where 2 KB boxes stall at ~4.9 TB/s.
+//   rows  = the G*T query rows of one kv head (padded to 16 for mma.sync
+//           m16n8k16; row r is query token r / G, head (kv head)*G + r % G).
 #include <math.h>
+
+#include <algorithm>
 
 #include "kernels.h"
 #include "plan_layout.h"
@@ -31,31 +40,12 @@
 namespace skd {
 namespace {
 
-constexpr int kBlockN = 64;
-constexpr int kCWarps = 4;
-constexpr int kThreads = (kCWarps + 1) * 32;
-constexpr int kCThreads = kCWarps * 32;
-
-template <int D>
-struct Smem {
-  static constexpr int kStages = 4;
-  static constexpr int kSub = D / 64;
-  static constexpr int kSubBytes = kBlockN * 128;
-  static constexpr int kTileBytes = kSub * kSubBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
-  static constexpr int kQBytes = 16 * D * 2;
-  static constexpr int kOStride = D + 8;  // floats; padding keeps fragment stores conflict-free
-  static constexpr int kQOff = kStages * kStageBytes;
-  static constexpr int kOOff = kQOff + 2 * kQBytes;
-  static constexpr int kMOff = kOOff + kCWarps * 16 * kOStride * 4;
-  static constexpr int kLOff = kMOff + kCWarps * 16 * 4;   // sum of bf16-rounded p
-  static constexpr int kLfOff = kLOff + kCWarps * 16 * 4;  // sum of fp32 p
-  static constexpr int kBarOff = kLfOff + kCWarps * 16 * 4;
-  static constexpr int kNumBars = 2 * kStages + 4;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kBytes = kMiscOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
-};
+constexpr int kMaxHG = 8;
+constexpr int kMaxStages = 8;
+constexpr int kFan = 8;  // splits folded per merge-tree node
+constexpr int kTraceWords = SKD_TRACE_RECORD_BYTES / 8;
+constexpr int kSmemBudget = 227 * 1024;
+constexpr float kLn2 = 0.69314718055994531f;
 
 struct Params {
   const __nv_bfloat16 *q;
@@ -63,156 +53,278 @@ struct Params {
   const int32_t *seqlens;
   const int32_t *plan;
   int32_t *err;
-  int32_t *counters;
+  int32_t *item_cnt;   // one per item
+  int32_t *group_cnt;  // one per slot (used at the first slot of each run of kFan)
   float *partials;
   __nv_bfloat16 *out;
   float *lse;
-  int batch, T, Hq, Hkv, G, P, max_pages, num_pages, causal, rows, max_slots;
+  int batch, T, Hq, Hkv, HG, NG, G, P, max_pages, num_pages, causal, rows, max_slots;
+  int nst, nq;  // pipeline stages, Q slots
+  int stage_bytes, tile_bytes, q_bytes, q_off, zero_off, bar_off, misc_off;
   float scale_log2;
-  int64_t slot_floats;
+  int64_t slot_floats, head_floats;
+  long long *trace;
 };
 
-__device__ __forceinline__ float fmax4(float a, float b, float c, float d) {
-  return fmaxf(fmaxf(a, b), fmaxf(c, d));
+// Merge `n` partial states of head h (slots base, base+stride, ...) in slot
+// order with a running maximum. Final: write out/lse rows; otherwise write the
+// folded state into slot `base`. One warp: 8 lanes per row (4 rows at a time),
+// each lane owning D/8 consecutive columns; 4 splits are loaded per step so
+// that a merge costs a few L2 round trips rather than one per split and row.
+template <int D>
+__device__ void merge_head(const Params &p, int h, int base, int n, int stride, bool final_out,
+                           int b, int head, int lane) {
+  constexpr int C4 = D / 32;  // float4 per lane per row (D/8 floats)
+  constexpr int U = 4;        // splits in flight
+  const int rows = p.rows;
+  const int rg = lane >> 3, cl = lane & 7;
+  for (int r0 = 0; r0 < rows; r0 += 4) {
+    const int r = r0 + rg;
+    const bool act = r < rows;
+    float M = -INFINITY, lam = 0.f, lamf = 0.f;
+    float4 acc[C4];
+#pragma unroll
+    for (int c = 0; c < C4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n; s0 += U) {
+      float mv[U], lv[U], lfv[U];
+      float4 ov[U][C4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        mv[u] = -INFINITY;
+        lv[u] = lfv[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < C4; ++c) ov[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (act && s0 + u < n) {
+          const float *ps = p.partials + int64_t(base + (s0 + u) * stride) * p.slot_floats + h * p.head_floats;
+          mv[u] = __ldcg(ps + rows * D + r);
+          lv[u] = __ldcg(ps + rows * D + rows + r);
+          lfv[u] = __ldcg(ps + rows * D + 2 * rows + r);
+          const float4 *o = reinterpret_cast<const float4 *>(ps + r * D + cl * (D / 8));
+#pragma unroll
+          for (int c = 0; c < C4; ++c) ov[u][c] = __ldcg(o + c);
+        }
+      }
+      float Mn = M;
+#pragma unroll
+      for (int u = 0; u < U; ++u) Mn = fmaxf(Mn, mv[u]);
+      const float Mu = Mn == -INFINITY ? 0.f : Mn;
+      const float sc = exp2f(M - Mu);
+      lam *= sc;
+      lamf *= sc;
+#pragma unroll
+      for (int c = 0; c < C4; ++c) {
+        acc[c].x *= sc;
+        acc[c].y *= sc;
+        acc[c].z *= sc;
+        acc[c].w *= sc;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float f = exp2f(mv[u] - Mu);
+        lam += lv[u] * f;
+        lamf += lfv[u] * f;
+#pragma unroll
+        for (int c = 0; c < C4; ++c) {
+          acc[c].x += ov[u][c].x * f;
+          acc[c].y += ov[u][c].y * f;
+          acc[c].z += ov[u][c].z * f;
+          acc[c].w += ov[u][c].w * f;
+        }
+      }
+      M = Mn;
+    }
+    __syncwarp();  // every lane has read slot `base` before it is overwritten
+    if (!act) continue;
+    if (final_out) {
+      const int t = r / p.G;
+      const int64_t orow = (int64_t(b) * p.T + t) * p.Hq + int64_t(head) * p.G + (r - t * p.G);
+      const float inv = 1.f / lam;
+      uint32_t pk[2 * C4];
+#pragma unroll
+      for (int c = 0; c < C4; ++c) {
+        pk[2 * c] = ptx::pack_bf16(acc[c].x * inv, acc[c].y * inv);
+        pk[2 * c + 1] = ptx::pack_bf16(acc[c].z * inv, acc[c].w * inv);
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + cl * (D / 8));
+#pragma unroll
+      for (int c = 0; c < C4 / 2; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      if (cl == 0) p.lse[orow] = (M + log2f(lamf)) * kLn2;
+    } else {
+      float *pd = p.partials + int64_t(base) * p.slot_floats + h * p.head_floats;
+      float4 *o = reinterpret_cast<float4 *>(pd + r * D + cl * (D / 8));
+#pragma unroll
+      for (int c = 0; c < C4; ++c) o[c] = acc[c];
+      if (cl == 0) {
+        pd[rows * D + r] = M;
+        pd[rows * D + rows + r] = lam;
+        pd[rows * D + 2 * rows + r] = lamf;
+      }
+    }
+  }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const Params p) {
-  using S = Smem<D>;
+  constexpr int NH = D / 64;  // 128-byte halves of a row
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int HG = p.HG;
   const int32_t *plan = p.plan;
 
   // A plan built for another launch is rejected by every thread alike.
-  if (plan[PH_MAGIC] != kPlanMagic || plan[PH_BATCH] != p.batch || plan[PH_HKV] != p.Hkv ||
+  if (plan[PH_MAGIC] != kPlanMagic || plan[PH_BATCH] != p.batch || plan[PH_NGRP] != p.NG ||
       plan[PH_NCTAS] != int(gridDim.x) || plan[PH_GRANULE] != kGranule ||
       plan[PH_NSLOTS] > p.max_slots || plan[PH_ERR] != 0) {
     if (threadIdx.x == 0) atomicOr(p.err, plan[PH_ERR] != 0 ? plan[PH_ERR] : SKD_DEVERR_PLAN);
     return;
   }
-  const PlanOffsets off = plan_offsets(p.batch, p.Hkv, gridDim.x);
+  const PlanOffsets off = plan_offsets(p.batch, p.NG, gridDim.x);
   const int seg_lo = plan[off.cta_off + blockIdx.x];
   const int seg_hi = plan[off.cta_off + blockIdx.x + 1];
   const int4 *segs = reinterpret_cast<const int4 *>(plan + off.segs);
 
   const uint32_t sbase = ptx::smem_u32(smem);
-  const uint32_t bar0 = sbase + S::kBarOff;
+  const uint32_t bar0 = sbase + p.bar_off;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (S::kStages + s); };
-  auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * S::kStages + s); };
-  auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * S::kStages + 2 + s); };
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kMiscOff);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+  auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStages + s); };
+  auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStages + 2 + s); };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.misc_off);
   volatile int *last_flag = abort_flag + 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S::kStages; ++s) {
+    for (int s = 0; s < p.nst; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), kCWarps);
+      ptx::mbar_init(empty_bar(s), HG);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < p.nq; ++s) {
       ptx::mbar_init(qfull_bar(s), 1);
-      ptx::mbar_init(qempty_bar(s), kCWarps);
+      ptx::mbar_init(qempty_bar(s), HG);
     }
     *abort_flag = 0;
     *last_flag = 0;
     ptx::fence_mbar_init();
   }
-  // Q slots: rows beyond G*T stay zero for the whole kernel.
-  {
-    int4 *qz = reinterpret_cast<int4 *>(smem + S::kQOff);
-    for (int i = threadIdx.x; i < 2 * S::kQBytes / 16; i += kThreads) qz[i] = make_int4(0, 0, 0, 0);
-    ptx::fence_proxy_async_smem();
-  }
+  // a zero row: A-fragment rows beyond G*T read it
+  for (int i = threadIdx.x; i < D * 2 / 16; i += blockDim.x)
+    reinterpret_cast<int4 *>(smem + p.zero_off)[i] = make_int4(0, 0, 0, 0);
   __syncthreads();
 
-  const int Hkv = p.Hkv, G = p.G, T = p.T, rows = p.rows;
+  const int NG = p.NG, G = p.G, T = p.T, rows = p.rows;
+  long long *const tr = p.trace ? p.trace + int64_t(blockIdx.x) * kTraceWords : nullptr;
+  if (tr && threadIdx.x == 0) tr[0] = (long long)ptx::globaltimer_ns();
+  const long long t_begin = clock64();
+  long long t_wait = 0;  // cycles this warp spent in barrier waits (trace only)
 
   // =========================== producer ====================================
-  if (warp == kCWarps) {
-    if (lane != 0) return;
-    ptx::prefetch_tmap(&tmK);
-    ptx::prefetch_tmap(&tmV);
+  // The whole warp walks the segments; lane 0 waits on barriers and issues the
+  // copies. Page ids of 32 granules are fetched with one coalesced warp load
+  // and handed to lane 0 by shuffles.
+  if (warp == HG) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmK);
+      ptx::prefetch_tmap(&tmV);
+    }
     const uint64_t pol = ptx::policy_evict_first();
     int stage = 0, qs = 0;
     uint32_t phase = 0, qph = 0;
-    uint32_t last_parity_mask = 0, used_mask = 0;  // for the final drain
+    uint32_t last_parity_mask = 0, used_mask = 0;
     bool ok = true;
     for (int si = seg_lo; si < seg_hi && ok; ++si) {
       const int4 sg = segs[si];
       const int item = sg.x, tb = sg.y, te = sg.z;
       if (te <= tb) continue;
-      const int b = item / Hkv, h = item - b * Hkv;
-      const int L = p.seqlens[b];
-      if (te > L || L > p.max_pages * p.P || (p.causal && L < T)) atomicOr(p.err, SKD_DEVERR_SEQLEN);
-      if (!ptx::mbar_wait(qempty_bar(qs), qph ^ 1u, abort_flag, kWaitCycles)) {
-        ok = false;
-        break;
+      const int b = item / NG, head0 = (item - b * NG) * HG;
+      if (lane == 0) {
+        const int L = p.seqlens[b];
+        if (te > L || L > p.max_pages * p.P || (p.causal && L < T)) atomicOr(p.err, SKD_DEVERR_SEQLEN);
+        const long long w0 = clock64();
+        const bool got = ptx::mbar_wait(qempty_bar(qs), qph ^ 1u, abort_flag, kWaitCycles);
+        t_wait += clock64() - w0;
+        if (!got) {
+          ok = false;
+        } else {
+          const uint32_t per_t = uint32_t(HG * G * D * 2);
+          ptx::mbar_arrive_expect_tx(qfull_bar(qs), per_t * T);
+          for (int t = 0; t < T; ++t)
+            ptx::bulk_load(sbase + p.q_off + qs * p.q_bytes + t * per_t,
+                           p.q + ((int64_t(b) * T + t) * p.Hq + int64_t(head0) * G) * D, per_t,
+                           qfull_bar(qs));
+        }
       }
-      ptx::mbar_arrive_expect_tx(qfull_bar(qs), uint32_t(rows * D * 2));
-      for (int t = 0; t < T; ++t) {
-        const __nv_bfloat16 *src = p.q + ((int64_t(b) * T + t) * p.Hq + int64_t(h) * G) * D;
-        ptx::bulk_load(sbase + S::kQOff + qs * S::kQBytes + t * G * D * 2, src, uint32_t(G * D * 2),
-                       qfull_bar(qs));
-      }
-      if (++qs == 2) {
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (++qs == p.nq) {
         qs = 0;
         qph ^= 1u;
       }
       const int32_t *ptab = p.page_table + int64_t(b) * p.max_pages;
-      for (int tok0 = tb; tok0 < te; tok0 += kBlockN) {
-        if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitCycles)) {
-          ok = false;
-          break;
-        }
-        const int ng = min(kBlockN / kGranule, (te - tok0 + kGranule - 1) / kGranule);
-        ptx::mbar_arrive_expect_tx(full_bar(stage), uint32_t(ng * kGranule * 2 * D * 2));
-        const uint32_t kdst = sbase + stage * S::kStageBytes;
-        const uint32_t vdst = kdst + S::kTileBytes;
-        for (int gi = 0; gi < ng; ++gi) {
-          const int tok = tok0 + gi * kGranule;
-          const int j = tok / p.P, slot = tok - j * p.P;
-          int pg = j < p.max_pages ? ptab[j] : -1;
+      for (int c0 = tb; c0 < te && ok; c0 += 32 * kGranule) {
+        const int tk = c0 + lane * kGranule;
+        int pg = 0;
+        if (tk < te) {
+          const int j = tk / p.P;
+          pg = j < p.max_pages ? __ldg(ptab + j) : -1;
           if (pg < 0 || pg >= p.num_pages) {
             atomicOr(p.err, SKD_DEVERR_PAGE);
             pg = 0;
           }
-#pragma unroll
-          for (int sub = 0; sub < S::kSub; ++sub) {
-            const uint32_t o = sub * S::kSubBytes + gi * kGranule * 128;
-            ptx::tma_load_4d(kdst + o, &tmK, full_bar(stage), sub * 64, h, slot, pg, pol);
-            ptx::tma_load_4d(vdst + o, &tmV, full_bar(stage), sub * 64, h, slot, pg, pol);
-          }
         }
-        used_mask |= 1u << stage;
-        last_parity_mask = (last_parity_mask & ~(1u << stage)) | (phase << stage);
-        if (++stage == S::kStages) {
-          stage = 0;
-          phase ^= 1u;
+        const int cend = min(te, c0 + 32 * kGranule);
+        for (int tok0 = c0; tok0 < cend; tok0 += kGranule) {
+          const int pgi = __shfl_sync(0xffffffffu, pg, (tok0 - c0) / kGranule);
+          if (lane == 0) {
+            const long long w0 = clock64();
+            const bool got = ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitCycles);
+            t_wait += clock64() - w0;
+            if (!got) {
+              ok = false;
+            } else {
+              ptx::mbar_arrive_expect_tx(full_bar(stage), uint32_t(p.stage_bytes));
+              const uint32_t kdst = sbase + stage * p.stage_bytes;
+              const int slot = tok0 % p.P;
+              ptx::tma_load_5d(kdst, &tmK, full_bar(stage), 0, slot, 0, head0, pgi, pol);
+              ptx::tma_load_5d(kdst + p.tile_bytes, &tmV, full_bar(stage), 0, slot, 0, head0, pgi, pol);
+              used_mask |= 1u << stage;
+              last_parity_mask = (last_parity_mask & ~(1u << stage)) | (phase << stage);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (++stage == p.nst) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
-    if (!ok) *abort_flag = 1, atomicOr(p.err, SKD_DEVERR_TIMEOUT);
-    // Drain: every fill this thread issued must have landed before the CTA
-    // may exit (normally the consumers have already waited for all of them).
-    for (int s = 0; s < S::kStages; ++s)
-      if (used_mask & (1u << s))
-        ptx::mbar_wait(full_bar(s), (last_parity_mask >> s) & 1u, nullptr, kWaitCycles);
+    if (lane == 0) {
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, SKD_DEVERR_TIMEOUT);
+      }
+      // every fill this warp issued must land before the CTA may exit
+      for (int s = 0; s < p.nst; ++s)
+        if (used_mask & (1u << s))
+          ptx::mbar_wait(full_bar(s), (last_parity_mask >> s) & 1u, nullptr, kWaitCycles);
+      if (tr) {
+        tr[4] = t_wait;
+        tr[5] = clock64() - t_begin;
+      }
+    }
     return;
   }
 
   // =========================== consumers ===================================
-  const int w = warp;
-  const int tid = threadIdx.x;  // 0..127
-  const int fr = lane >> 2;     // fragment row (and row + 8)
-  const int fc = lane & 3;      // fragment column pair
-  float *sm_o = reinterpret_cast<float *>(smem + S::kOOff);
-  float *sm_m = reinterpret_cast<float *>(smem + S::kMOff);
-  float *sm_l = reinterpret_cast<float *>(smem + S::kLOff);
-  float *sm_lf = reinterpret_cast<float *>(smem + S::kLfOff);
+  const int h = warp;            // head within the group
+  const int ctid = threadIdx.x;  // 0 .. HG*32-1
+  const int cthreads = HG * 32;
+  const int fr = lane >> 2, fc = lane & 3;
+  const int r0 = fr, r1 = fr + 8;
   const float NEG_INF = -INFINITY;
   int stage = 0, qs = 0;
   uint32_t phase = 0, qph = 0;
@@ -220,48 +332,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int si = seg_lo; si < seg_hi; ++si) {
     const int4 sg = segs[si];
     const int item = sg.x, tb = sg.y, te = sg.z, wslot = sg.w;
-    const int b = item / Hkv, h = item - b * Hkv;
-    // combine-phase mapping: thread -> (row, 1/8 of the columns)
-    const int cr = tid >> 3;
-    const int cb = (tid & 7) * (D / 8);
-    const int ct = cr < rows ? cr / G : 0;
-    const int64_t orow = ((int64_t(b) * T + ct) * p.Hq + int64_t(h) * G + (cr - ct * G));
+    const int b = item / NG;
+    const int head = (item - b * NG) * HG + h;
+    auto out_row = [&](int r) {
+      const int t = r / G;
+      return (int64_t(b) * T + t) * p.Hq + int64_t(head) * G + (r - t * G);
+    };
 
     if (te <= tb) {  // empty request: out = 0, lse = -inf
-      if (cr < rows) {
-        int4 *o4 = reinterpret_cast<int4 *>(p.out + orow * D + cb);
-#pragma unroll
-        for (int i = 0; i < D / 64; ++i) o4[i] = make_int4(0, 0, 0, 0);
-        if ((tid & 7) == 0) p.lse[orow] = NEG_INF;
+      for (int i = lane; i < rows * (D / 8); i += 32) {
+        const int r = i / (D / 8), c = i - r * (D / 8);
+        reinterpret_cast<int4 *>(p.out + out_row(r) * D)[c] = make_int4(0, 0, 0, 0);
       }
+      for (int r = lane; r < rows; r += 32) p.lse[out_row(r)] = NEG_INF;
       continue;
     }
     const int L = p.seqlens[b];
 
-    // ---- Q fragments (A operand, rows x D) ----
+    // ---- Q fragments (A operand, 16 x D; rows >= G*T read the zero row) ----
     uint32_t qa[D / 16][4];
     bool alive = !*abort_flag;
-    if (alive && !ptx::mbar_wait(qfull_bar(qs), qph, abort_flag, kWaitCycles)) {
-      alive = false;
-      *abort_flag = 1;
+    {
+      const long long w0 = clock64();
+      if (alive && !ptx::mbar_wait(qfull_bar(qs), qph, abort_flag, kWaitCycles)) {
+        alive = false;
+        *abort_flag = 1;
+      }
+      t_wait += clock64() - w0;
     }
     if (alive) {
-      const uint32_t qb = sbase + S::kQOff + qs * S::kQBytes;
       const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      uint32_t rb;
+      if (r < rows) {
+        const int t = r / G;
+        rb = sbase + p.q_off + qs * p.q_bytes + ((t * HG + h) * G + (r - t * G)) * (D * 2);
+      } else {
+        rb = sbase + p.zero_off;
+      }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        ptx::ldsm_x4(qb + r * D * 2 + (2 * kk + (lane >> 4)) * 16, qa[kk][0], qa[kk][1], qa[kk][2],
-                     qa[kk][3]);
+        ptx::ldsm_x4(rb + (2 * kk + (lane >> 4)) * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      // The Q slot is refilled by TMA as soon as every warp has arrived on
+      // qempty, so the fragments must be in registers first: reading them
+      // makes in-order issue wait for the loads, and the proxy fence orders
+      // these generic reads before the async-proxy writes of the refill.
+      uint32_t dep = 0;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) dep |= qa[kk][0] | qa[kk][1] | qa[kk][2] | qa[kk][3];
+      asm volatile("" ::"r"(dep));
+      ptx::fence_proxy_async_smem();
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(qempty_bar(qs));
-    if (++qs == 2) {
+    if (++qs == p.nq) {
       qs = 0;
       qph ^= 1u;
     }
 
-    // last visible key of fragment rows fr and fr + 8 (causal: L - T + t)
-    const int r0 = fr, r1 = fr + 8;
+    // last visible key of fragment rows r0 and r1 (causal: L - T + t)
     const int lim0 = (p.causal && r0 < rows) ? L - T + r0 / G : INT_MAX;
     const int lim1 = (p.causal && r1 < rows) ? L - T + r1 / G : INT_MAX;
 
@@ -272,42 +400,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     // exact convex combination of V rows); lf: sum of fp32 p (gives lse)
     float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f, lf0 = 0.f, lf1 = 0.f;
 
-    for (int tok0 = tb; tok0 < te; tok0 += kBlockN) {
-      if (alive && !ptx::mbar_wait(full_bar(stage), phase, abort_flag, kWaitCycles)) {
-        alive = false;
-        *abort_flag = 1;
+    for (int tok0 = tb; tok0 < te; tok0 += kGranule) {
+      {
+        const long long w0 = clock64();
+        if (alive && !ptx::mbar_wait(full_bar(stage), phase, abort_flag, kWaitCycles)) {
+          alive = false;
+          *abort_flag = 1;
+        }
+        t_wait += clock64() - w0;
+        if (tr && lane == 0 && h == 0) atomicAdd(reinterpret_cast<unsigned long long *>(tr + 7), 1ull);
       }
-      const int mytok = tok0 + w * kGranule;
-      if (alive && mytok < te) {
-        const uint32_t kb = sbase + stage * S::kStageBytes;
-        const uint32_t vb = kb + S::kTileBytes;
-        if (mytok + kGranule > te) {
+      if (alive) {
+        const uint32_t kb = sbase + stage * p.stage_bytes + h * (NH * kGranule * 128);
+        const uint32_t vb = kb + p.tile_bytes;
+        if (tok0 + kGranule > te) {
           // rows past the end of the request hold arbitrary bytes: zero their V
-          const int r_lo = te - mytok;
-          const int chunks = (kGranule - r_lo) * S::kSub * 8;
-          for (int c = lane; c < chunks; c += 32) {
-            const int rr = r_lo + c / (S::kSub * 8);
-            const int rest = c % (S::kSub * 8);
-            const int sub = rest >> 3, ch = rest & 7;
-            int4 *dst = reinterpret_cast<int4 *>(smem + stage * S::kStageBytes + S::kTileBytes +
-                                                 sub * S::kSubBytes + (w * kGranule + rr) * 128 +
-                                                 ch * 16);
-            *dst = make_int4(0, 0, 0, 0);
+          const int t_lo = te - tok0;
+          const int per_half = (kGranule - t_lo) * 8;
+          uint8_t *vrow = smem + stage * p.stage_bytes + p.tile_bytes + h * (NH * kGranule * 128);
+          for (int c = lane; c < per_half * NH; c += 32) {
+            const int hh = c / per_half;
+            const int rest = c - hh * per_half;
+            const int t = t_lo + (rest >> 3);
+            *reinterpret_cast<int4 *>(vrow + (hh * kGranule + t) * 128 + (rest & 7) * 16) =
+                make_int4(0, 0, 0, 0);
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
         }
-        // ---- S = Q K^T over this warp's 16 tokens ----
+        // ---- S = Q K^T over the 16 tokens ----
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
-          const int trow = w * kGranule + ((lane >> 4) << 3) + (lane & 7);
-          const uint32_t rbase = kb + trow * 128;
-          const int sw = trow & 7;
+          const int t = (lane & 7) + ((lane >> 4) << 3);
+          const int sw = t & 7;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const int ch = 2 * (kk & 3) + ((lane >> 3) & 1);
+            const int c = 2 * (kk & 3) + ((lane >> 3) & 1);
             uint32_t b0, b1, b2, b3;
-            ptx::ldsm_x4(rbase + (kk >> 2) * S::kSubBytes + ((ch ^ sw) << 4), b0, b1, b2, b3);
+            ptx::ldsm_x4(kb + ((kk >> 2) * kGranule + t) * 128 + ((c ^ sw) << 4), b0, b1, b2, b3);
             ptx::mma_bf16_16816(s[0], qa[kk], b0, b1);
             ptx::mma_bf16_16816(s[1], qa[kk], b2, b3);
           }
@@ -318,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int tok = mytok + 8 * j + 2 * fc + e;
+            const int tok = tok0 + 8 * j + 2 * fc + e;
             const bool in = tok < te;
             s[j][e] = (in && tok <= lim0) ? s[j][e] * p.scale_log2 : NEG_INF;
             s[j][2 + e] = (in && tok <= lim1) ? s[j][2 + e] * p.scale_log2 : NEG_INF;
@@ -364,14 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- O += P V ----
         {
-          const int trow = w * kGranule + (lane & 7) + (((lane >> 3) & 1) << 3);
-          const uint32_t rbase = vb + trow * 128;
-          const int sw = trow & 7;
+          const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int sw = t & 7;
 #pragma unroll
           for (int jj = 0; jj < D / 16; ++jj) {
-            const int chg = 2 * jj + (lane >> 4);  // 8-column chunk of V
+            const int cg = 2 * jj + (lane >> 4);  // 8-column chunk of V
             uint32_t b0, b1, b2, b3;
-            ptx::ldsm_x4_t(rbase + (chg >> 3) * S::kSubBytes + (((chg & 7) ^ sw) << 4), b0, b1, b2,
+            ptx::ldsm_x4_t(vb + ((cg >> 3) * kGranule + t) * 128 + (((cg & 7) ^ sw) << 4), b0, b1, b2,
                            b3);
             ptx::mma_bf16_16816(o[2 * jj], pa, b0, b1);
             ptx::mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
@@ -380,13 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(empty_bar(stage));
-      if (++stage == S::kStages) {
+      if (++stage == p.nst) {
         stage = 0;
         phase ^= 1u;
       }
     }
 
-    // ---- merge the four warps' states of this segment ----
+    // ---- this warp's head is complete for the segment ----
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -395,145 +524,122 @@ __global__ void __launch_bounds__(kThreads, 1)
     lf0 += __shfl_xor_sync(0xffffffffu, lf0, 2);
     lf1 += __shfl_xor_sync(0xffffffffu, lf1, 1);
     lf1 += __shfl_xor_sync(0xffffffffu, lf1, 2);
-    if (fc == 0) {
-      sm_m[w * 16 + r0] = m0;
-      sm_m[w * 16 + r1] = m1;
-      sm_l[w * 16 + r0] = l0;
-      sm_l[w * 16 + r1] = l1;
-      sm_lf[w * 16 + r0] = lf0;
-      sm_lf[w * 16 + r1] = lf1;
-    }
-    {
-      float *ow = sm_o + w * 16 * S::kOStride;
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        *reinterpret_cast<float2 *>(ow + r0 * S::kOStride + 8 * j + 2 * fc) = make_float2(o[j][0], o[j][1]);
-        *reinterpret_cast<float2 *>(ow + r1 * S::kOStride + 8 * j + 2 * fc) = make_float2(o[j][2], o[j][3]);
-      }
-    }
-    ptx::named_bar(1, kCThreads);
-
     const bool split = wslot >= 0;
-    const bool live = !*abort_flag;
-    float acc[D / 8];
-    float M = NEG_INF, Lt = 0.f, Lf = 0.f;
-    if (cr < rows && live) {
-#pragma unroll
-      for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, sm_m[ww * 16 + cr]);
-      const float Mu = M == NEG_INF ? 0.f : M;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < kCWarps; ++ww) {
-        const float f = exp2f(sm_m[ww * 16 + cr] - Mu);
-        Lt += sm_l[ww * 16 + cr] * f;
-        Lf += sm_lf[ww * 16 + cr] * f;
-        const float *src = sm_o + (ww * 16 + cr) * S::kOStride + cb;
-#pragma unroll
-        for (int c = 0; c < D / 8; c += 4) {
-          const float4 v = *reinterpret_cast<const float4 *>(src + c);
-          acc[c] += v.x * f;
-          acc[c + 1] += v.y * f;
-          acc[c + 2] += v.z * f;
-          acc[c + 3] += v.w * f;
-        }
-      }
+    if (alive) {
       if (!split) {
-        const float inv = 1.f / Lt;
-        uint32_t pk[D / 16];
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
+        const int64_t o0 = r0 < rows ? out_row(r0) * D : -1, o1 = r1 < rows ? out_row(r1) * D : -1;
 #pragma unroll
-        for (int c = 0; c < D / 8; c += 2) pk[c / 2] = ptx::pack_bf16(acc[c] * inv, acc[c + 1] * inv);
-        int4 *o4 = reinterpret_cast<int4 *>(p.out + orow * D + cb);
-#pragma unroll
-        for (int i = 0; i < D / 64; ++i) o4[i] = make_int4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        if ((tid & 7) == 0) p.lse[orow] = (M + log2f(Lf)) * 0.69314718055994531f;
+        for (int j = 0; j < D / 8; ++j) {
+          if (o0 >= 0)
+            *reinterpret_cast<uint32_t *>(p.out + o0 + 8 * j + 2 * fc) = ptx::pack_bf16(o[j][0] * i0, o[j][1] * i0);
+          if (o1 >= 0)
+            *reinterpret_cast<uint32_t *>(p.out + o1 + 8 * j + 2 * fc) = ptx::pack_bf16(o[j][2] * i1, o[j][3] * i1);
+        }
+        if (fc == 0) {
+          if (r0 < rows) p.lse[out_row(r0)] = (m0 + log2f(lf0)) * kLn2;
+          if (r1 < rows) p.lse[out_row(r1)] = (m1 + log2f(lf1)) * kLn2;
+        }
       } else {
-        float *ps = p.partials + int64_t(wslot) * p.slot_floats;
-        float4 *d4 = reinterpret_cast<float4 *>(ps + cr * D + cb);
+        float *ps = p.partials + int64_t(wslot) * p.slot_floats + h * p.head_floats;
 #pragma unroll
-        for (int c = 0; c < D / 8; c += 4) d4[c / 4] = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-        if ((tid & 7) == 0) {
-          ps[rows * D + cr] = M;
-          ps[rows * D + rows + cr] = Lt;
-          ps[rows * D + 2 * rows + cr] = Lf;
+        for (int j = 0; j < D / 8; ++j) {
+          if (r0 < rows) *reinterpret_cast<float2 *>(ps + r0 * D + 8 * j + 2 * fc) = make_float2(o[j][0], o[j][1]);
+          if (r1 < rows) *reinterpret_cast<float2 *>(ps + r1 * D + 8 * j + 2 * fc) = make_float2(o[j][2], o[j][3]);
+        }
+        if (fc == 0) {
+          if (r0 < rows) {
+            ps[rows * D + r0] = m0;
+            ps[rows * D + rows + r0] = l0;
+            ps[rows * D + 2 * rows + r0] = lf0;
+          }
+          if (r1 < rows) {
+            ps[rows * D + r1] = m1;
+            ps[rows * D + rows + r1] = l1;
+            ps[rows * D + 2 * rows + r1] = lf1;
+          }
         }
       }
     }
     if (split) {
-      // publish the partial, count arrivals; the last split merges
+      // publish the partial and count arrivals; the last split merges
+      const int nsp = plan[off.nsplit + item];
+      const int s0 = plan[off.slot0 + item];
+      const int sidx = wslot - s0;
       __threadfence();
-      ptx::named_bar(1, kCThreads);
-      if (tid == 0) {
+      ptx::named_bar(1, cthreads);
+      if (ctid == 0) {
         int last = 0;
         if (!*abort_flag) {
-          const int nsp = plan[off.nsplit + item];
-          const int old = atomicAdd(p.counters + item, 1);
-          last = (old == nsp - 1) ? 1 : 0;
+          if (nsp <= kFan) {
+            last = atomicAdd(p.item_cnt + item, 1) == nsp - 1 ? 2 : 0;
+          } else {
+            const int k = sidx / kFan;
+            const int gsz = min(kFan, nsp - k * kFan);
+            last = atomicAdd(p.group_cnt + s0 + k * kFan, 1) == gsz - 1 ? 1 : 0;
+          }
         }
         *last_flag = last;
       }
-      ptx::named_bar(1, kCThreads);
-      if (*last_flag) {
+      ptx::named_bar(1, cthreads);
+      int last = *last_flag;
+      if (last == 1) {  // fold this run of kFan splits into its first slot
         __threadfence();
-        const int nsp = plan[off.nsplit + item];
-        const int s0 = plan[off.slot0 + item];
-        if (cr < rows) {
-          float Mx = NEG_INF;
-          for (int s = 0; s < nsp; ++s)
-            Mx = fmaxf(Mx, __ldcg(p.partials + int64_t(s0 + s) * p.slot_floats + rows * D + cr));
-          const float Mu = Mx == NEG_INF ? 0.f : Mx;
-          float lam = 0.f, lamf = 0.f;
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
-          for (int s = 0; s < nsp; ++s) {
-            const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats;
-            const float f = exp2f(__ldcg(ps + rows * D + cr) - Mu);
-            lam += __ldcg(ps + rows * D + rows + cr) * f;
-            lamf += __ldcg(ps + rows * D + 2 * rows + cr) * f;
-            const float4 *src = reinterpret_cast<const float4 *>(ps + cr * D + cb);
-#pragma unroll
-            for (int c = 0; c < D / 8; c += 4) {
-              const float4 v = __ldcg(src + c / 4);
-              acc[c] += v.x * f;
-              acc[c + 1] += v.y * f;
-              acc[c + 2] += v.z * f;
-              acc[c + 3] += v.w * f;
-            }
-          }
-          const float inv = 1.f / lam;
-          uint32_t pk[D / 16];
-#pragma unroll
-          for (int c = 0; c < D / 8; c += 2) pk[c / 2] = ptx::pack_bf16(acc[c] * inv, acc[c + 1] * inv);
-          int4 *o4 = reinterpret_cast<int4 *>(p.out + orow * D + cb);
-#pragma unroll
-          for (int i = 0; i < D / 64; ++i)
-            o4[i] = make_int4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          if ((tid & 7) == 0) p.lse[orow] = (Mx + log2f(lamf)) * 0.69314718055994531f;
+        const int k = sidx / kFan;
+        const int gsz = min(kFan, nsp - k * kFan);
+        merge_head<D>(p, h, s0 + k * kFan, gsz, 1, false, b, head, lane);
+        __threadfence();
+        ptx::named_bar(1, cthreads);
+        if (ctid == 0) {
+          p.group_cnt[s0 + k * kFan] = 0;
+          const int ngroups = (nsp + kFan - 1) / kFan;
+          *last_flag = atomicAdd(p.item_cnt + item, 1) == ngroups - 1 ? 3 : 0;
         }
-        if (tid == 0) p.counters[item] = 0;
+        ptx::named_bar(1, cthreads);
+        last = *last_flag;
+      }
+      if (last >= 2) {  // final merge: all splits (2) or all runs (3)
+        __threadfence();
+        if (last == 2)
+          merge_head<D>(p, h, s0, nsp, 1, true, b, head, lane);
+        else
+          merge_head<D>(p, h, s0, (nsp + kFan - 1) / kFan, kFan, true, b, head, lane);
+        if (ctid == 0) p.item_cnt[item] = 0;
       }
     }
-    ptx::named_bar(1, kCThreads);  // shared scratch is reused by the next segment
+    ptx::named_bar(1, cthreads);  // last_flag is reused by the next segment
+  }
+  if (tr && lane == 0) {
+    atomicAdd(reinterpret_cast<unsigned long long *>(tr + 2), (unsigned long long)t_wait);
+    atomicAdd(reinterpret_cast<unsigned long long *>(tr + 3), (unsigned long long)(clock64() - t_begin));
+    if (h == 0) {
+      tr[6] = seg_hi - seg_lo;
+      tr[1] = (long long)ptx::globaltimer_ns();
+    }
   }
 }
 
 template <int D>
 int launch_d(const DecodeArgs &a) {
-  using S = Smem<D>;
+  constexpr int NH = D / 64;
   const skd_shape_t &s = a.shape;
+  const int HG = head_group(s.num_kv_heads);
+  const int G = s.num_q_heads / s.num_kv_heads;
   CUtensorMap tk, tv;
-  const cuuint64_t gk[4] = {cuuint64_t(D), cuuint64_t(s.num_kv_heads), cuuint64_t(s.page_size),
+  // dims (innermost first): 64 dims, page slot, 128-byte half, kv head, page
+  const cuuint64_t gd[5] = {64, cuuint64_t(s.page_size), cuuint64_t(NH), cuuint64_t(s.num_kv_heads),
                             cuuint64_t(s.num_pages)};
-  const cuuint64_t sk[3] = {cuuint64_t(D) * 2, cuuint64_t(s.num_kv_heads) * D * 2,
+  const cuuint64_t sk[4] = {cuuint64_t(s.num_kv_heads) * D * 2, 128, cuuint64_t(D) * 2,
                             cuuint64_t(s.page_size) * s.num_kv_heads * D * 2};
-  const cuuint64_t sv[3] = {cuuint64_t(s.v_row_stride) * 2, cuuint64_t(s.num_kv_heads) * s.v_row_stride * 2,
+  const cuuint64_t sv[4] = {cuuint64_t(s.num_kv_heads) * s.v_row_stride * 2, 128,
+                            cuuint64_t(s.v_row_stride) * 2,
                             cuuint64_t(s.page_size) * s.num_kv_heads * s.v_row_stride * 2};
-  const cuuint32_t box[4] = {64, 1, cuuint32_t(kGranule), 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  if (encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.k), gk, sk, box, es,
+  const cuuint32_t box[5] = {64, cuuint32_t(kGranule), cuuint32_t(NH), cuuint32_t(HG), 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  if (encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(a.k), gd, sk, box, es,
                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return SKD_EINVAL;
-  if (encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.v), gk, sv, box, es,
+  if (encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(a.v), gd, sv, box, es,
                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return SKD_EINVAL;
 
@@ -542,33 +648,57 @@ int launch_d(const DecodeArgs &a) {
   p.page_table = a.page_table;
   p.seqlens = a.seqlens;
   p.plan = a.plan;
-  p.err = static_cast<int32_t *>(a.ws);
-  p.counters = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(a.ws) + a.wl.counters);
-  p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(a.ws) + a.wl.partials);
+  uint8_t *ws = static_cast<uint8_t *>(a.ws);
+  p.err = reinterpret_cast<int32_t *>(ws);
+  p.item_cnt = reinterpret_cast<int32_t *>(ws + a.wl.counters);
+  p.group_cnt = reinterpret_cast<int32_t *>(ws + a.wl.group_counters);
+  p.partials = reinterpret_cast<float *>(ws + a.wl.partials);
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.lse = a.lse;
   p.batch = s.batch;
   p.T = s.q_tokens;
   p.Hq = s.num_q_heads;
   p.Hkv = s.num_kv_heads;
-  p.G = s.num_q_heads / s.num_kv_heads;
+  p.HG = HG;
+  p.NG = s.num_kv_heads / HG;
+  p.G = G;
   p.P = s.page_size;
   p.max_pages = s.max_pages_per_req;
   p.num_pages = s.num_pages;
   p.causal = s.causal ? 1 : 0;
-  p.rows = p.G * s.q_tokens;
+  p.rows = G * s.q_tokens;
   p.max_slots = int(a.wl.slots);
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.slot_floats = a.wl.slot_floats;
+  p.head_floats = a.wl.head_floats;
+  p.trace = static_cast<long long *>(trace_buffer(a.n_ctas));
 
-  static bool attr_set = false;  // per-process; the attribute is per function
+  // shared memory: stages | Q slots | zero row | barriers | flags
+  p.tile_bytes = HG * NH * kGranule * 128;
+  p.stage_bytes = 2 * p.tile_bytes;
+  p.q_bytes = ((HG * G * s.q_tokens * D * 2) + 127) / 128 * 128;
+  const int fixed = D * 2 + (2 * kMaxStages + 4) * 8 + 16 + 1024;
+  p.nq = 2;
+  p.nst = std::min(kMaxStages, (kSmemBudget - fixed - 2 * p.q_bytes) / p.stage_bytes);
+  if (p.nst < 3) {
+    p.nq = 1;
+    p.nst = std::min(kMaxStages, (kSmemBudget - fixed - p.q_bytes) / p.stage_bytes);
+  }
+  if (p.nst < 2) return SKD_EUNSUPPORTED;
+  p.q_off = p.nst * p.stage_bytes;
+  p.zero_off = p.q_off + p.nq * p.q_bytes;
+  p.bar_off = p.zero_off + D * 2;
+  p.misc_off = p.bar_off + (2 * kMaxStages + 4) * 8;
+  const int smem = p.misc_off + 16 + 1024;
+
+  static bool attr_set = false;  // per process; the attribute belongs to the function
   if (!attr_set) {
     if (cudaFuncSetAttribute(gqa_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             S::kAlloc) != cudaSuccess)
+                             kSmemBudget) != cudaSuccess)
       return SKD_ECUDA;
     attr_set = true;
   }
-  gqa_decode_kernel<D><<<a.n_ctas, kThreads, S::kAlloc, a.stream>>>(tk, tv, p);
+  gqa_decode_kernel<D><<<a.n_ctas, (HG + 1) * 32, smem, a.stream>>>(tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

@@ -8,12 +8,14 @@
 
 namespace skd {
 
-// Workspace layout: [0,256) error word; counters (one int32 per item);
-// partial-state slots (2 per CTA), each holding O[rows][Dv], m[rows], l[rows],
-// lf[rows] in fp32 (m in log2 units of the scaled score; l sums the bf16-rounded
-// probabilities that entered P.V, lf the fp32 ones).
+// Workspace layout: [0,256) error word; item counters (one int32 per
+// (request, kv-head group) item); merge-tree counters (one int32 per slot);
+// partial-state slots (2 per CTA). A slot holds, for each head of the group, a
+// block of head_floats floats: O[rows][Dv], m[rows], l[rows], lf[rows] (m in
+// log2 units of the scaled score; l sums the bf16-rounded probabilities that
+// entered P.V, lf the fp32 ones).
 struct WsLayout {
-  int64_t counters, partials, slot_floats, slots, bytes;
+  int64_t counters, group_counters, partials, slot_floats, head_floats, slots, bytes;
   int rows;
 };
 WsLayout ws_layout(const skd_shape_t &s, int n_ctas);
@@ -32,13 +34,17 @@ struct DecodeArgs {
 
 int launch_gqa(const DecodeArgs &a);
 int launch_mla(const DecodeArgs &a);
-int launch_plan_device(const int32_t *seqlens, int batch, int hkv, int n_ctas, int32_t *plan,
+int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n_ctas, int32_t *plan,
                        cudaStream_t stream);
 
 // cuTensorMapEncodeTiled, looked up through the runtime (no libcuda link).
 CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, cuuint32_t rank, void *gaddr,
                       const cuuint64_t *gdim, const cuuint64_t *gstride, const cuuint32_t *box,
                       const cuuint32_t *estride, CUtensorMapSwizzle swz);
+
+// Per-CTA timing records enabled by skd_trace_enable (nullptr when off or when
+// the buffer is too small for n_ctas records).
+void *trace_buffer(int n_ctas);
 
 // Bounded device waits give up after this many SM cycles (about one second).
 constexpr long long kWaitCycles = 2000000000LL;

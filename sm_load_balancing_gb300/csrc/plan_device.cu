@@ -66,7 +66,7 @@ __device__ int block_exclusive_scan(int32_t *a, int len, int32_t *warp_sums, int
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
-    plan_device_kernel(const int32_t *__restrict__ seqlens, int batch, int hkv, int n,
+    plan_device_kernel(const int32_t *__restrict__ seqlens, int batch, int ngrp, int n,
                        int32_t *__restrict__ plan) {
   extern __shared__ int32_t sm[];
   int32_t *req_pref = sm;                 // [batch + 1] granule prefix per request
@@ -76,8 +76,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   __shared__ int32_t carry;
   __shared__ int32_t err;
   const int tid = threadIdx.x;
-  const PlanOffsets off = plan_offsets(batch, hkv, n);
-  const int64_t items = int64_t(batch) * hkv;
+  const PlanOffsets off = plan_offsets(batch, ngrp, n);
+  const int64_t items = int64_t(batch) * ngrp;
   int32_t *nsplit = plan + off.nsplit;
   int32_t *slot0 = plan + off.slot0;
   int4 *segs = reinterpret_cast<int4 *>(plan + off.segs);
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   const int32_t req_total = block_exclusive_scan(req_pref, batch, warp_sums, &carry);
   if (tid == 0) req_pref[batch] = req_total;
   __syncthreads();
-  const int64_t total = int64_t(hkv) * req_pref[batch];
+  const int64_t total = int64_t(ngrp) * req_pref[batch];
   if (tid == 0 && total > 0x7fffffffLL) err |= SKD_DEVERR_SEQLEN;
   __syncthreads();
   if (err) {
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     if (tid == 0) {
       plan[PH_MAGIC] = kPlanMagic;
       plan[PH_BATCH] = batch;
-      plan[PH_HKV] = hkv;
+      plan[PH_NGRP] = ngrp;
       plan[PH_NCTAS] = n;
       plan[PH_GRANULE] = kGranule;
       plan[PH_ERR] = err;
@@ -115,9 +115,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 
   // pass 1: per item, the CTAs it touches; count segments per CTA
   for (int64_t i = tid; i < items; i += kPlanThreads) {
-    const int b = int(i / hkv), h = int(i - int64_t(b) * hkv);
+    const int b = int(i / ngrp), h = int(i - int64_t(b) * ngrp);
     const int64_t g = req_pref[b + 1] - req_pref[b];
-    const int64_t s = int64_t(hkv) * req_pref[b] + h * g, e = s + g;
+    const int64_t s = int64_t(ngrp) * req_pref[b] + h * g, e = s + g;
     int ns = 0;
     if (g == 0) {
       const int64_t c = cta_of(s, total, n);
@@ -147,10 +147,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   __syncthreads();
   // pass 2: write segments
   for (int64_t i = tid; i < items; i += kPlanThreads) {
-    const int b = int(i / hkv), h = int(i - int64_t(b) * hkv);
+    const int b = int(i / ngrp), h = int(i - int64_t(b) * ngrp);
     const int L = seqlens[b];
     const int64_t g = req_pref[b + 1] - req_pref[b];
-    const int64_t s = int64_t(hkv) * req_pref[b] + h * g, e = s + g;
+    const int64_t s = int64_t(ngrp) * req_pref[b] + h * g, e = s + g;
     const int ns = nsplit[i];
     const int sl0 = ns > 1 ? slot0[i] : -1;
     if (g == 0) {
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     for (int j = 0; j < PH_WORDS; ++j) plan[j] = 0;
     plan[PH_MAGIC] = kPlanMagic;
     plan[PH_BATCH] = batch;
-    plan[PH_HKV] = hkv;
+    plan[PH_NGRP] = ngrp;
     plan[PH_NCTAS] = n;
     plan[PH_GRANULE] = kGranule;
     plan[PH_NITEMS] = int(items);
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 
 }  // namespace
 
-int launch_plan_device(const int32_t *seqlens, int batch, int hkv, int n, int32_t *plan,
+int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n, int32_t *plan,
                        cudaStream_t stream) {
   const size_t smem = size_t(batch + 1 + 2 * (n + 1)) * 4;
   if (smem > 200 * 1024) return SKD_EUNSUPPORTED;
@@ -203,7 +203,7 @@ int launch_plan_device(const int32_t *seqlens, int batch, int hkv, int n, int32_
       cudaFuncSetAttribute(plan_device_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return SKD_ECUDA;
-  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seqlens, batch, hkv, n, plan);
+  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seqlens, batch, ngrp, n, plan);
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

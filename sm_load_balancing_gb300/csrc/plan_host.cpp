@@ -6,7 +6,7 @@
 // tail wave waits on a slow CTA. "MeldKernel：动态负载下跨 SM 融合内核（SOSP 2026）",
 // core method: the mapping is decided at run time from the actual lengths.
 //
-// Work item i = b*Hkv + h carries ceil(L_b / 16) granules; CTA c receives the
+// Work item i = b*NGRP + g (kv-head group g) carries ceil(L_b / 16) granules; CTA c receives the
 // granule range [floor(c*G/n), floor((c+1)*G/n)) of the items laid end to end,
 // cut at item boundaries. A single linear sweep, O(items + n).
 #include <string.h>
@@ -20,18 +20,18 @@ namespace skd {
 
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int build_plan_host(const int32_t *seqlens, int batch, int hkv, int page_size, int n, int mode,
+int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, int n, int mode,
                     void *plan_out, size_t plan_bytes) {
   if (!seqlens && batch > 0) return SKD_EINVAL;
-  if (!plan_out || batch < 0 || hkv <= 0 || n <= 0) return SKD_EINVAL;
+  if (!plan_out || batch < 0 || ngrp <= 0 || n <= 0) return SKD_EINVAL;
   if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
   if (mode != SKD_PLAN_STREAMK && mode != SKD_PLAN_ROUND_ROBIN) return SKD_EINVAL;
-  const PlanOffsets off = plan_offsets(batch, hkv, n);
+  const PlanOffsets off = plan_offsets(batch, ngrp, n);
   if (plan_bytes < size_t(off.words) * 4) return SKD_EPLAN;
   for (int b = 0; b < batch; ++b)
     if (seqlens[b] < 0) return SKD_EINVAL;
 
-  const int64_t items = int64_t(batch) * hkv;
+  const int64_t items = int64_t(batch) * ngrp;
   const int64_t cap = items + n;
   int32_t *w = static_cast<int32_t *>(plan_out);
   memset(w, 0, size_t(off.words) * 4);
@@ -41,7 +41,7 @@ int build_plan_host(const int32_t *seqlens, int batch, int hkv, int page_size, i
   int32_t *slot0 = w + off.slot0;
 
   int64_t total = 0;
-  for (int b = 0; b < batch; ++b) total += int64_t(hkv) * ceil_div(seqlens[b], kGranule);
+  for (int b = 0; b < batch; ++b) total += int64_t(ngrp) * ceil_div(seqlens[b], kGranule);
   if (total > INT32_MAX) return SKD_EPLAN;
 
   int64_t nseg = 0;
@@ -66,7 +66,7 @@ int build_plan_host(const int32_t *seqlens, int batch, int hkv, int page_size, i
       }
     };
     for (int64_t i = 0; i < items; ++i) {
-      const int64_t L = seqlens[i / hkv];
+      const int64_t L = seqlens[i / ngrp];
       const int64_t g = ceil_div(L, kGranule);
       const int64_t s = pos, e = pos + g;
       pos = e;
@@ -97,7 +97,7 @@ int build_plan_host(const int32_t *seqlens, int batch, int hkv, int page_size, i
     // round robin: item i -> CTA i mod n, no splits
     for (int64_t c = 0; c < n; ++c) {
       cta_off[c] = int32_t(nseg);
-      for (int64_t i = c; i < items; i += n) push(i, 0, seqlens[i / hkv]);
+      for (int64_t i = c; i < items; i += n) push(i, 0, seqlens[i / ngrp]);
     }
     cta_off[n] = int32_t(nseg);
   }
@@ -119,7 +119,7 @@ int build_plan_host(const int32_t *seqlens, int batch, int hkv, int page_size, i
 
   w[PH_MAGIC] = kPlanMagic;
   w[PH_BATCH] = batch;
-  w[PH_HKV] = hkv;
+  w[PH_NGRP] = ngrp;
   w[PH_NCTAS] = n;
   w[PH_GRANULE] = kGranule;
   w[PH_NITEMS] = int32_t(items);

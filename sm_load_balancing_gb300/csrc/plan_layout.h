@@ -4,7 +4,7 @@
 //   [0, 16)                  header (PH_*)
 //   cta_seg_offset[n+1]      segments of CTA c are [off[c], off[c+1])
 //   segs[cap][4]             {item, tok_begin, tok_end, slot}, 16-byte aligned;
-//                            item = b*Hkv + h; slot = -1 when the segment is the
+//                            item = b*NGRP + g (g = kv-head group); slot = -1 when the segment is the
 //                            whole item, else its workspace slot for partials
 //   item_nsplit[num_items]   number of segments of each item
 //   item_slot0[num_items]    slot of split 0 (splits use consecutive slots)
@@ -20,13 +20,20 @@
 
 namespace skd {
 
+// kv heads handled together by one CTA: the largest divisor of Hkv not above 8
+SKD_HD inline int head_group(int hkv) {
+  for (int g = hkv < 8 ? hkv : 8; g > 1; --g)
+    if (hkv % g == 0) return g;
+  return 1;
+}
+
 constexpr int32_t kPlanMagic = 0x534B4431;  // "SKD1"
 constexpr int kGranule = 16;
 
 enum PlanHeader : int {
   PH_MAGIC = 0,
   PH_BATCH = 1,
-  PH_HKV = 2,
+  PH_NGRP = 2,  // work items per request (kv-head groups)
   PH_NCTAS = 3,
   PH_GRANULE = 4,
   PH_NITEMS = 5,

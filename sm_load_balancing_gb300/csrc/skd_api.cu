@@ -11,7 +11,7 @@
 #include "skdecode.h"
 
 namespace skd {
-int build_plan_host(const int32_t *seqlens, int batch, int hkv, int page_size, int n, int mode,
+int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, int n, int mode,
                     void *plan_out, size_t plan_bytes);
 
 namespace {
@@ -21,6 +21,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
+
+void *g_trace = nullptr;
+size_t g_trace_bytes = 0;
 
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -42,6 +45,10 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, cuuint32_t rank,
                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+void *trace_buffer(int n_ctas) {
+  return (g_trace && g_trace_bytes >= size_t(n_ctas) * SKD_TRACE_RECORD_BYTES) ? g_trace : nullptr;
+}
+
 // rows per (request, kv head) item: every query row that reads that kv head
 static int item_rows(const skd_shape_t &s) {
   return (s.num_q_heads / s.num_kv_heads) * s.q_tokens;
@@ -49,12 +56,15 @@ static int item_rows(const skd_shape_t &s) {
 
 WsLayout ws_layout(const skd_shape_t &s, int n_ctas) {
   WsLayout w;
-  const int64_t items = int64_t(s.batch) * s.num_kv_heads;
+  const int hg = head_group(s.num_kv_heads);
+  const int64_t items = int64_t(s.batch) * (s.num_kv_heads / hg);
   w.rows = item_rows(s);
-  w.counters = 256;
-  w.partials = align_up(w.counters + 4 * items, 256);
-  w.slot_floats = align_up(int64_t(w.rows) * (s.head_dim_v + 3), 4);
   w.slots = 2 * int64_t(n_ctas);
+  w.counters = 256;
+  w.group_counters = align_up(w.counters + 4 * items, 256);
+  w.partials = align_up(w.group_counters + 4 * w.slots, 256);
+  w.head_floats = align_up(int64_t(w.rows) * (s.head_dim_v + 3), 4);
+  w.slot_floats = w.head_floats * hg;
   w.bytes = w.partials + w.slots * w.slot_floats * 4;
   return w;
 }
@@ -114,13 +124,15 @@ int skd_device_sm_count(int device, int *sm_count_out) {
 
 size_t skd_plan_bytes(int batch, int num_kv_heads, int n_ctas) {
   if (batch < 0 || num_kv_heads < 1 || n_ctas < 1) return 0;
-  return size_t(plan_offsets(batch, num_kv_heads, n_ctas).words) * 4;
+  const int ngrp = num_kv_heads / head_group(num_kv_heads);
+  return size_t(plan_offsets(batch, ngrp, n_ctas).words) * 4;
 }
 
 int skd_decode_plan(const int32_t *seqlens_host, int batch, int num_kv_heads, int page_size,
                     int n_ctas, int mode, void *plan_host, size_t plan_bytes) {
-  return build_plan_host(seqlens_host, batch, num_kv_heads, page_size, n_ctas, mode, plan_host,
-                         plan_bytes);
+  if (num_kv_heads < 1) return SKD_EINVAL;
+  return build_plan_host(seqlens_host, batch, num_kv_heads / head_group(num_kv_heads), page_size,
+                         n_ctas, mode, plan_host, plan_bytes);
 }
 
 int skd_decode_plan_device(const int32_t *seqlens_dev, int batch, int num_kv_heads, int page_size,
@@ -130,7 +142,7 @@ int skd_decode_plan_device(const int32_t *seqlens_dev, int batch, int num_kv_hea
   if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
   if (!aligned(plan_dev, 16)) return SKD_EINVAL;
   if (plan_bytes < skd_plan_bytes(batch, num_kv_heads, n_ctas)) return SKD_EPLAN;
-  return launch_plan_device(seqlens_dev, batch, num_kv_heads, n_ctas,
+  return launch_plan_device(seqlens_dev, batch, num_kv_heads / head_group(num_kv_heads), n_ctas,
                             static_cast<int32_t *>(plan_dev), static_cast<cudaStream_t>(stream));
 }
 
@@ -178,6 +190,13 @@ int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_
   a.lse = lse;
   a.stream = static_cast<cudaStream_t>(stream);
   return shape->kind == SKD_KIND_GQA ? launch_gqa(a) : launch_mla(a);
+}
+
+int skd_trace_enable(void *trace_dev, size_t bytes) {
+  if (trace_dev && !aligned(trace_dev, 8)) return SKD_EINVAL;
+  g_trace = trace_dev;
+  g_trace_bytes = trace_dev ? bytes : 0;
+  return SKD_OK;
 }
 
 int skd_read_error(const void *ws, int32_t *err_out, void *stream) {

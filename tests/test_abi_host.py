@@ -54,11 +54,18 @@ def _host_plan(N, seqlens, hkv, n, mode=0, page_size=16):
     return st, buf
 
 
+def head_groups(hkv):
+    """kv-head groups per request: heads go together in groups of the largest
+    divisor of hkv not above 8 (the rule include/skdecode.h states)."""
+    hg = max(g for g in range(1, min(hkv, 8) + 1) if hkv % g == 0)
+    return hkv // hg
+
+
 def _check_against_oracle(N, seqlens, hkv, n):
     st, buf = _host_plan(N, seqlens, hkv, n)
     assert st == 0
     p = PD.decode(buf)
-    ref = S.streamk_split(seqlens, hkv, n, granule=16)
+    ref = S.streamk_split(seqlens, head_groups(hkv), n, granule=16)
     got = [[(i, tb, te) for i, tb, te, _ in segs] for segs in p["segments"]]
     assert got == ref["segments"]
     assert p["total"] == ref["total_granules"]
@@ -87,7 +94,7 @@ def _check_against_oracle(N, seqlens, hkv, n):
 def test_host_planner_equals_streamk_definition(N, seed):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(0, 9))
-    hkv = int(rng.integers(1, 5))
+    hkv = int(rng.choice([1, 2, 3, 4, 8, 9, 10, 12, 16, 24, 32]))
     n = int(rng.choice([1, 2, 3, 7, 13, 148, 152, 304]))
     seqlens = [int(x) for x in rng.integers(0, 400, size=B)]
     if B and seed % 3 == 0:
@@ -106,9 +113,13 @@ def test_host_planner_on_named_workloads(N, name, n):
     assert max(per) - min(per) <= 1
 
 
+def test_head_group_rule():
+    assert [head_groups(h) for h in [1, 2, 4, 7, 8, 9, 12, 16, 32]] == [1, 1, 1, 1, 1, 3, 2, 2, 4]
+
+
 def test_round_robin_mode_matches_definition(N):
     seqlens = [5, 0, 9, 100, 33]
-    st, buf = _host_plan(N, seqlens, 2, 4, mode=1)
+    st, buf = _host_plan(N, seqlens, 16, 4, mode=1)   # 16 kv heads -> 2 groups of 8
     assert st == 0
     p = PD.decode(buf)
     ref = S.round_robin_split(seqlens, 2, 4)
@@ -139,9 +150,11 @@ def test_workspace_bytes(N):
     lib = N.lib()
     s = _shape(N)
     nb = lib.skd_workspace_bytes(ctypes.byref(s), 148)
-    rows = 4
-    slot = -(-rows * 67 // 4) * 4
-    assert nb == 256 + 256 + 2 * 148 * slot * 4  # counters fit in the first 256-byte block
+    rows, hg = 4, 2
+    head = -(-rows * 67 // 4) * 4
+    group_counters = 512
+    partials = group_counters + -(-(4 * 2 * 148) // 256) * 256
+    assert nb == partials + 2 * 148 * head * hg * 4
     assert lib.skd_workspace_bytes(ctypes.byref(_shape(N, head_dim_qk=96, head_dim_v=96,
                                                        v_row_stride=96)), 148) == 0
     assert lib.skd_workspace_bytes(ctypes.byref(_shape(N, num_q_heads=64, num_kv_heads=2)), 8) == 0

@@ -37,6 +37,11 @@ MEDIUM = [
          page_size=32),
     dict(seqlens=[513, 1024, 40], q_tokens=3, causal=False, num_q_heads=20, num_kv_heads=4,
          head_dim_qk=128, page_size=16),
+    # kv heads in groups of 6 (two groups per request) and of 8 (two groups)
+    dict(seqlens=[260, 1500, 31], num_q_heads=24, num_kv_heads=12, head_dim_qk=64, page_size=16),
+    dict(seqlens=[900, 77, 2222], q_tokens=2, num_q_heads=32, num_kv_heads=16, head_dim_qk=128,
+         page_size=32),
+    dict(seqlens=[333, 64], num_q_heads=9, num_kv_heads=3, head_dim_qk=128, page_size=16),
 ]
 
 
@@ -202,3 +207,14 @@ def test_skewed_long_request_first_and_last():
     for seq in ([40000] + short, short + [40000]):
         w = W.make_custom(seq, num_q_heads=64, num_kv_heads=8, head_dim_qk=128, page_size=64, seed=2)
         _check(w)
+
+
+@pytest.mark.parametrize("n_ctas", [8, 9, 16, 17, 152])
+def test_merge_tree_fan_in(n_ctas):
+    """One long request split over every CTA: 8 splits merge in one level,
+    9 and more go through the two-level tree."""
+    w = W.make_custom([6000], num_q_heads=32, num_kv_heads=8, head_dim_qk=128, page_size=16, seed=n_ctas)
+    _check(w, n_ctas=n_ctas)
+    w2 = W.make_custom([3000, 5], q_tokens=4, num_q_heads=32, num_kv_heads=8, head_dim_qk=128,
+                       page_size=16, seed=n_ctas)
+    _check(w2, n_ctas=n_ctas)
