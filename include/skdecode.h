@@ -184,11 +184,13 @@ int skd_read_error(const void *ws_dev, int32_t *err_out, void *stream);
  * words {0: %globaltimer ns at start, 1: ns at end, 2: consumer cycles spent
  * waiting for data (summed over consumer warps), 3: consumer cycles in total
  * (summed), 4: producer cycles waiting for free stages, 5: producer cycles in
- * total, 6: segments, 7: pipeline stages}. Words 2, 3 and 7 are accumulated
- * with atomics: zero the buffer before each launch. A buffer smaller than
+ * total, 6: segments, 7: pipeline stages, 8: SM id, 9: consumer cycles spent
+ * publishing and merging partial states (summed), 10: final merges, 11:
+ * merge-tree node merges, 12..15: reserved}. Words 2, 3, 7, 9, 10 and 11 are
+ * accumulated with atomics: zero the buffer before each launch. A buffer smaller than
  * n_ctas records disables tracing for that launch. Process-wide setting, not
  * thread-safe; pass NULL to disable. Errors: SKD_EINVAL (misaligned pointer). */
-#define SKD_TRACE_RECORD_BYTES 64
+#define SKD_TRACE_RECORD_BYTES 128
 int skd_trace_enable(void *trace_dev, size_t bytes);
 
 #ifdef __cplusplus

@@ -11,8 +11,8 @@
 // the split that arrives last merges the partials right there
 // ("MeldKernel：动态负载下跨 SM 融合内核（SOSP 2026）", core method:
 // just-in-time reduction, no separate reduction kernel and no wait for the
-// slowest split). Items with more than 8 splits merge as a two-level tree:
-// the last arriver of each run of 8 consecutive splits folds them into one
+// slowest split). Items with more than 16 splits merge as a two-level tree:
+// the last arriver of each run of 16 consecutive splits folds them into one
 // partial, and the last of those runs folds the runs. Nobody waits for
 // another CTA, so the kernel is correct for any grid size and any scheduling
 // order.
@@ -42,7 +42,7 @@ namespace {
 
 constexpr int kMaxHG = 8;
 constexpr int kMaxStages = 8;
-constexpr int kFan = 8;  // splits folded per merge-tree node
+constexpr int kFan = 16;  // splits folded per merge-tree node
 constexpr int kTraceWords = SKD_TRACE_RECORD_BYTES / 8;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr float kLn2 = 0.69314718055994531f;
@@ -69,13 +69,13 @@ struct Params {
 // Merge `n` partial states of head h (slots base, base+stride, ...) in slot
 // order with a running maximum. Final: write out/lse rows; otherwise write the
 // folded state into slot `base`. One warp: 8 lanes per row (4 rows at a time),
-// each lane owning D/8 consecutive columns; 4 splits are loaded per step so
+// each lane owning D/8 consecutive columns; 4-8 splits are loaded per step so
 // that a merge costs a few L2 round trips rather than one per split and row.
 template <int D>
 __device__ void merge_head(const Params &p, int h, int base, int n, int stride, bool final_out,
                            int b, int head, int lane) {
   constexpr int C4 = D / 32;  // float4 per lane per row (D/8 floats)
-  constexpr int U = 4;        // splits in flight
+  constexpr int U = D >= 128 ? 4 : 8;  // splits in flight (register budget: 168/thread)
   const int rows = p.rows;
   const int rg = lane >> 3, cl = lane & 7;
   for (int r0 = 0; r0 < rows; r0 += 4) {
@@ -218,7 +218,8 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
   long long *const tr = p.trace ? p.trace + int64_t(blockIdx.x) * kTraceWords : nullptr;
   if (tr && threadIdx.x == 0) tr[0] = (long long)ptx::globaltimer_ns();
   const long long t_begin = clock64();
-  long long t_wait = 0;  // cycles this warp spent in barrier waits (trace only)
+  long long t_wait = 0;   // cycles this warp spent in barrier waits (trace only)
+  long long t_merge = 0;  // cycles this warp spent publishing and merging partials
 
   // =========================== producer ====================================
   // The whole warp walks the segments; lane 0 waits on barriers and issues the
@@ -562,58 +563,66 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
       }
     }
     if (split) {
-      // publish the partial and count arrivals; the last split merges
+      // Publish the partial and count arrivals; the last split merges. The
+      // barrier orders every consumer thread's partial writes before thread
+      // 0's release-acquire atomic, which publishes them GPU-wide.
+      const long long tm0 = clock64();
       const int nsp = plan[off.nsplit + item];
       const int s0 = plan[off.slot0 + item];
       const int sidx = wslot - s0;
-      __threadfence();
+      const int k = sidx / kFan;
       ptx::named_bar(1, cthreads);
       if (ctid == 0) {
         int last = 0;
         if (!*abort_flag) {
           if (nsp <= kFan) {
-            last = atomicAdd(p.item_cnt + item, 1) == nsp - 1 ? 2 : 0;
+            last = ptx::atom_add_acq_rel_gpu(p.item_cnt + item, 1) == nsp - 1 ? 2 : 0;
           } else {
-            const int k = sidx / kFan;
             const int gsz = min(kFan, nsp - k * kFan);
-            last = atomicAdd(p.group_cnt + s0 + k * kFan, 1) == gsz - 1 ? 1 : 0;
+            last = ptx::atom_add_acq_rel_gpu(p.group_cnt + s0 + k * kFan, 1) == gsz - 1 ? 1 : 0;
           }
         }
         *last_flag = last;
       }
       ptx::named_bar(1, cthreads);
       int last = *last_flag;
+      auto merge = [&](int mbase, int mn, int mstride, bool fin) {
+        merge_head<D>(p, h, mbase, mn, mstride, fin, b, head, lane);
+      };
       if (last == 1) {  // fold this run of kFan splits into its first slot
-        __threadfence();
-        const int k = sidx / kFan;
         const int gsz = min(kFan, nsp - k * kFan);
-        merge_head<D>(p, h, s0 + k * kFan, gsz, 1, false, b, head, lane);
-        __threadfence();
+        merge(s0 + k * kFan, gsz, 1, false);
         ptx::named_bar(1, cthreads);
         if (ctid == 0) {
+          if (tr) atomicAdd(reinterpret_cast<unsigned long long *>(tr + 11), 1ull);
           p.group_cnt[s0 + k * kFan] = 0;
           const int ngroups = (nsp + kFan - 1) / kFan;
-          *last_flag = atomicAdd(p.item_cnt + item, 1) == ngroups - 1 ? 3 : 0;
+          *last_flag = ptx::atom_add_acq_rel_gpu(p.item_cnt + item, 1) == ngroups - 1 ? 3 : 0;
         }
         ptx::named_bar(1, cthreads);
         last = *last_flag;
       }
       if (last >= 2) {  // final merge: all splits (2) or all runs (3)
-        __threadfence();
         if (last == 2)
-          merge_head<D>(p, h, s0, nsp, 1, true, b, head, lane);
+          merge(s0, nsp, 1, true);
         else
-          merge_head<D>(p, h, s0, (nsp + kFan - 1) / kFan, kFan, true, b, head, lane);
-        if (ctid == 0) p.item_cnt[item] = 0;
+          merge(s0, (nsp + kFan - 1) / kFan, kFan, true);
+        if (ctid == 0) {
+          p.item_cnt[item] = 0;
+          if (tr) atomicAdd(reinterpret_cast<unsigned long long *>(tr + 10), 1ull);
+        }
       }
+      t_merge += clock64() - tm0;
     }
     ptx::named_bar(1, cthreads);  // last_flag is reused by the next segment
   }
   if (tr && lane == 0) {
     atomicAdd(reinterpret_cast<unsigned long long *>(tr + 2), (unsigned long long)t_wait);
     atomicAdd(reinterpret_cast<unsigned long long *>(tr + 3), (unsigned long long)(clock64() - t_begin));
+    atomicAdd(reinterpret_cast<unsigned long long *>(tr + 9), (unsigned long long)t_merge);
     if (h == 0) {
       tr[6] = seg_hi - seg_lo;
+      tr[8] = ptx::smid();
       tr[1] = (long long)ptx::globaltimer_ns();
     }
   }

@@ -60,9 +60,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+__device__ __forceinline__ int smid() {
+  int v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
+
 // ---- proxy fences ------------------------------------------------------------
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ---- TMA ---------------------------------------------------------------------
@@ -152,6 +161,16 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 }
 
 __device__ __forceinline__ float ld_cg_f32(const float *p) { return __ldcg(p); }
+
+// Atomic add with acquire-release semantics at GPU scope: the release half
+// publishes every write this thread has observed (cumulative, so writes of
+// other threads ordered before it by a CTA barrier are included); the acquire
+// half makes other CTAs' released writes visible to what follows.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
 
 }  // namespace ptx
 }  // namespace skd
