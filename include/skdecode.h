@@ -175,6 +175,29 @@ int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_
 /* Copy the device error word to *err_out (synchronises `stream`). */
 int skd_read_error(const void *ws_dev, int32_t *err_out, void *stream);
 
+/* Allocation-free variant of skd_decode_attention (GQA only), for callers
+ * that cannot allocate device memory for a workspace: operator plugins whose
+ * fixed interface has no scratch argument, or runtimes whose device memory is
+ * planned up front and may not grow. The pages have no counterpart; this is an
+ * interface convenience. The workspace is a fixed 32 MiB module-scope device
+ * array that every GPU loading this library holds until the process exits.
+ * Arguments are those of skd_decode_attention without ws/ws_bytes; the caller
+ * still owns q, the cache, page table, seqlens, plan, out and lse.
+ * Errors: SKD_ESIZE when skd_workspace_bytes(shape, n_ctas) exceeds 32 MiB
+ * (nothing is enqueued); SKD_EUNSUPPORTED for MLA; SKD_ECUDA if the array's
+ * device address cannot be obtained. The first call on a device looks that
+ * address up (cudaGetSymbolAddress), so make it before any stream capture.
+ * Each call clears the array's error word and counters on `stream`, then
+ * launches. All calls share the one array, which keeps the last call's
+ * contents: calls that overlap on the GPU (other streams, other threads)
+ * race and give wrong results; serialise them. Device-side error bits land
+ * in the shared array and are not reported; use skd_decode_attention with a
+ * workspace to diagnose. */
+int skd_decode_attention_noalloc(const skd_shape_t *shape, const void *q, const void *k_pages,
+                                 const void *v_pages, const int32_t *page_table,
+                                 const int32_t *seqlens, const void *plan_dev, int n_ctas, void *out,
+                                 float *lse, void *stream);
+
 /* ---- diagnostics ------------------------------------------------------- */
 
 /* Per-CTA execution trace, after the GLM-5.2 decode article's Kineto analysis

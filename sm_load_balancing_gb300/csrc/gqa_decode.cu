@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kernels.h"
 #include "plan_layout.h"
@@ -723,3 +724,56 @@ int launch_gqa(const DecodeArgs &a) {
 }
 
 }  // namespace skd
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point. Some callers cannot allocate device memory for
+// a workspace: operator plugins whose fixed interface has no scratch argument,
+// or runtimes whose memory is planned up front by a framework allocator that
+// forbids further cudaMalloc calls. For them the workspace (error word,
+// arrival counters, partial softmax states) lives in a fixed module-scope
+// device array of kNoAllocScratchBytes, which every GPU that loads this library
+// holds until the process exits.
+namespace skd {
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];  // device address of the array, per device
+}  // namespace
+
+}  // namespace skd
+
+extern "C" int skd_decode_attention_noalloc(const skd_shape_t *shape, const void *q,
+                                            const void *k_pages, const void *v_pages,
+                                            const int32_t *page_table, const int32_t *seqlens,
+                                            const void *plan_dev, int n_ctas, void *out,
+                                            float *lse, void *stream) {
+  using namespace skd;
+  if (!shape || shape->kind != SKD_KIND_GQA) return shape ? SKD_EUNSUPPORTED : SKD_EINVAL;
+  const size_t need = skd_workspace_bytes(shape, n_ctas);
+  if (need == 0) return n_ctas < 1 ? SKD_EINVAL : SKD_EUNSUPPORTED;
+  if (need > kNoAllocScratchBytes) return SKD_ESIZE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SKD_ECUDA;
+  void *ws = nullptr;
+  {
+    // first call on this device: look up the array's device address (host code
+    // only sees a host-side stand-in for the symbol)
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SKD_ECUDA;
+      g_noalloc_ptr[dev] = ptr;
+    }
+    ws = g_noalloc_ptr[dev];
+  }
+  // the error word and the counters must start at zero; the partial slots are
+  // always written before they are read
+  const WsLayout wl = ws_layout(*shape, n_ctas);
+  if (cudaMemsetAsync(ws, 0, size_t(wl.partials), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SKD_ECUDA;
+  return skd_decode_attention(shape, q, k_pages, v_pages, page_table, seqlens, plan_dev, n_ctas, ws,
+                              kNoAllocScratchBytes, out, lse, stream);
+}
+
