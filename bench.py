@@ -248,8 +248,8 @@ def run_ours(a):
     v = None if w.mla else bf16(w.v_pages).to(dev)
     pt = torch.from_numpy(w.page_table).to(dev)
     sl = torch.from_numpy(w.seqlens).to(dev)
-    n = a.n_ctas or skd.sm_count()
     shape = skd.make_shape(q, k, v, pt, scale=w.scale, causal=w.causal)
+    n = a.n_ctas or skd.default_ctas(shape)
     plan_h = skd.plan(w.seqlens, shape.num_kv_heads, w.page_size, n, a.mode)
     plan_d = plan_h.to(dev)
     ws = skd.workspace(shape, n, dev)

@@ -23,7 +23,7 @@ from ._native import (SKD_DEVERR_PAGE, SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN,
                       SKD_DEVERR_TIMEOUT, SKD_GRANULE, SkdError)
 
 __all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention", "read_error",
-           "sm_count", "make_shape", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
+           "sm_count", "default_ctas", "make_shape", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
            "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT"]
 
 _MODES = {"streamk": N.SKD_PLAN_STREAMK, "round_robin": N.SKD_PLAN_ROUND_ROBIN}
@@ -39,6 +39,13 @@ def sm_count(device: Optional[int] = None) -> int:
     v = ctypes.c_int(0)
     N.check("skd_device_sm_count", N.lib().skd_device_sm_count(dev, ctypes.byref(v)))
     return v.value
+
+
+def default_ctas(shape: Optional[N.Shape] = None, device: Optional[int] = None) -> int:
+    """Stream-K workers for one wave: one per SM for GQA; for absorbed MLA a
+    worker is a 2-CTA cluster, so half the SMs."""
+    n = sm_count(device)
+    return n // 2 if (shape is not None and shape.kind == N.SKD_KIND_MLA) else n
 
 
 def plan_bytes(batch: int, num_kv_heads: int, n_ctas: int) -> int:

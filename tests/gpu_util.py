@@ -30,7 +30,7 @@ class Dev:
 
     def run(self, n_ctas=None, mode="streamk", plan=None, ws=None, out=None, lse=None):
         skd = self.skd
-        n = skd.sm_count() if n_ctas is None else n_ctas
+        n = skd.default_ctas(self.shape) if n_ctas is None else n_ctas
         if plan is None:
             plan = skd.plan(self.w.seqlens, self.shape.num_kv_heads, self.w.page_size, n, mode).cuda()
         if ws is None:
