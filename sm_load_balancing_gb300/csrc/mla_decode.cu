@@ -16,12 +16,11 @@
 //   rank 0 streams latent columns [0, 256), rank 1 columns [256, 576), one TMA
 //   box per 64-token block each (no byte is read twice);
 //   S = Q K^T: each rank computes the partial sum over its own columns
-//   (M=128 heads, N=64 tokens) into TMEM; the partner's half of the rows goes
-//   over DSMEM, so rank 0 owns the softmax of heads 0-63 and rank 1 of heads
-//   64-127, one thread per head row;
-//   P (bf16) and each row's rescale factor are written into both ranks' shared
-//   memory; O = P V: each rank accumulates its 256 value columns for all 128
-//   heads in TMEM (M=128, N=256, K=64 tokens).
+//   (M=128 heads, N=64 tokens) into TMEM and sends it to the partner over
+//   DSMEM; both ranks add the two partials (same bits: addition commutes) and
+//   run the same online softmax, one thread per head row;
+//   O = P V: each rank accumulates its 256 value columns for all 128 heads in
+//   TMEM (M=128, N=256, K=64 tokens) from its own copy of P.
 // The running maximum is kept per row and only moved (with an O rescale) when
 // a block's maximum exceeds it by more than 2^8, so p <= 256 and rescales are
 // rare; l and O stay consistent with the same reference maximum.
@@ -46,19 +45,19 @@ constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kTraceWords = SKD_TRACE_RECORD_BYTES / 8;
 
 // fixed shared-memory region (same offsets in both ranks, for DSMEM)
-constexpr int kOffP = 0;                     // P [128 rows][64 tok] bf16, SW128: 16 KB
-constexpr int kOffSx = 16384;                // partner's partial scores [64][64] fp32: 16 KB
-constexpr int kOffAlpha = 32768;             // per-row rescale factor [128] fp32
-constexpr int kOffStats = kOffAlpha + 512;   // m, l, lf [3][128] fp32
-constexpr int kOffBar = kOffStats + 1536;    // mbarriers
-constexpr int kNumBar = 2 * kMaxSt + 16;
+constexpr int kOffP = 0;                     // P [2 buffers][128 rows][64 tok] bf16, SW128: 32 KB
+constexpr int kOffSx = 32768;                // partner's partial scores [128][64] fp32: 32 KB
+constexpr int kOffBar = 65536;               // mbarriers
+constexpr int kNumBar = 2 * kMaxSt + 20;
 constexpr int kOffMisc = kOffBar + kNumBar * 8;  // tmem base, flags
-constexpr int kOffQ = 35 * 1024;             // Q [nch][128][128 B], then KV stages
+constexpr int kOffQ = 65 * 1024;             // Q [nch][128][128 B], then KV stages
 
 // barrier indices
+// (P buffers alternate per block; B_PF*, B_PVD* and B_OR* come in pairs, one per
+// buffer, so that no barrier can run two phases ahead of a waiter)
 enum {
   B_KVF = 0, B_KVE = kMaxSt, B_QF = 2 * kMaxSt, B_QE, B_SF0, B_SF1, B_SE0, B_SE1, B_SXF, B_SXFREE,
-  B_PF, B_PVD, B_OR, B_STF, B_PAIR, B_GO, B_FIN
+  B_PF0, B_PF1, B_PVD0, B_PVD1, B_OR0, B_OR1, B_STF, B_PAIR, B_GO, B_FIN
 };
 
 struct Params {
@@ -260,12 +259,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(cx.bar(B_SF1), 1);
     ptx::mbar_init(cx.bar(B_SE0), 4);
     ptx::mbar_init(cx.bar(B_SE1), 4);
-    ptx::mbar_init(cx.bar(B_SXF), 2);
-    ptx::mbar_init(cx.bar(B_SXFREE), 2);
-    ptx::mbar_init(cx.bar(B_PF), 4);
-    ptx::mbar_init(cx.bar(B_PVD), 2);
-    ptx::mbar_init(cx.bar(B_OR), 4);
-    ptx::mbar_init(cx.bar(B_STF), 4);
+    ptx::mbar_init(cx.bar(B_SXF), 4);
+    ptx::mbar_init(cx.bar(B_SXFREE), 4);
+    ptx::mbar_init(cx.bar(B_PF0), 4);
+    ptx::mbar_init(cx.bar(B_PF1), 4);
+    ptx::mbar_init(cx.bar(B_PVD0), 1);
+    ptx::mbar_init(cx.bar(B_PVD1), 1);
+    ptx::mbar_init(cx.bar(B_OR0), 4);
+    ptx::mbar_init(cx.bar(B_OR1), 4);
     ptx::mbar_init(cx.bar(B_PAIR), 1);
     ptx::mbar_init(cx.bar(B_GO), 1);
     ptx::mbar_init(cx.bar(B_FIN), 1);
@@ -285,8 +286,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tS[2] = {tmem + 0, tmem + 64};  // partial / full scores, double buffered
   const uint32_t tO = tmem + 128;                 // this rank's 256 value columns
 
-  long long *const tr = (p.trace && rank == 0) ? p.trace + int64_t(worker) * kTraceWords : nullptr;
+  // trace (when enabled): one record per CTA; words 2.. accumulate wait cycles
+  long long *const tr = p.trace ? p.trace + int64_t(blockIdx.x) * kTraceWords : nullptr;
   if (tr && threadIdx.x == 0) tr[0] = (long long)ptx::globaltimer_ns();
+  auto tw = [&](int idx, long long t0) {
+    if (tr && lane == 0) atomicAdd(reinterpret_cast<unsigned long long *>(tr + idx), (unsigned long long)(clock64() - t0));
+  };
+  const long long tk0 = clock64();
 
   if (warp == 0) {
     // ============================ TMA producer ===============================
@@ -319,7 +325,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             atomicOr(p.err, SKD_DEVERR_PAGE);
             pg = 0;
           }
+          const long long t0 = clock64();
           ok = cx.wait(B_KVE + st, ph ^ 1u);
+          tw(9, t0);
           if (ok) {
             ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + st), stage_bytes);
             tma3(sKV + st * stage_bytes, tkv, cx.bar(B_KVF + st), 0, pg * p.P + (w0 % p.P), chunk0, pol);
@@ -351,7 +359,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         auto issue_qk = [&](long long gg, int stage) {
           const int sb = int(gg & 1);
+          const long long t0 = clock64();
           if (!cx.wait(sb ? B_SE1 : B_SE0, uint32_t(((gg >> 1) & 1) ^ 1))) return false;
+          tw(8, t0);
           tc_fence_after();
           for (int c = 0; c < nch; ++c)
             for (int kk = 0; kk < 4; ++kk) {
@@ -376,27 +386,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ph_n ^= 1u;
           }
           if (j + 1 < nb) {
-            ok = cx.wait(B_KVF + st_n, ph_n) && issue_qk(g + 1, st_n);
+            const long long t0 = clock64();
+            ok = cx.wait(B_KVF + st_n, ph_n);
+            tw(6, t0);
+            ok = ok && issue_qk(g + 1, st_n);
             if (!ok) break;
           } else {
             umma_commit(cx.bar(B_QE));  // Q is free once this segment's last QK completes
           }
-          // PV of block j
-          if (!cx.wait(B_PF, uint32_t(g & 1)) || !cx.wait(B_OR, uint32_t(g & 1))) {
+          // PV of block j (P buffer g & 1)
+          const int pb = int(g & 1);
+          const long long t0 = clock64();
+          if (!cx.wait(B_PF0 + pb, uint32_t((g >> 1) & 1)) || !cx.wait(B_OR0 + pb, uint32_t((g >> 1) & 1))) {
             ok = false;
             break;
           }
-          // P rows arrived from both ranks through the generic proxy (some over
-          // DSMEM); the tensor core reads them through the async proxy
-          fence_proxy_async_all();
+          tw(7, t0);
           tc_fence_after();
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = sdesc(cx.sbase + kOffP + kk * 32, 16, 1024);
+            const uint64_t a = sdesc(cx.sbase + kOffP + pb * 16384 + kk * 32, 16, 1024);
             const uint64_t bd = sdesc(sKV + st_j * stage_bytes + kk * (16 * 128), kBlk * 128, 1024);
             umma(tO, a, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(cx.bar(B_KVE + st_j));
-          umma_commit_mc(cx.bar(B_PVD), 0x3);
+          umma_commit(cx.bar(B_PVD0 + pb));
           st_j = st_n;
           ph_j = ph_n;
           ++g;
@@ -410,16 +423,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================ epilogue warps =============================
+    // Each rank computes the softmax of all 128 rows: it sends its partial
+    // scores to the partner and adds the partner's, so both ranks hold the same
+    // full scores (fp32 addition commutes) and derive the same P, rescale
+    // factors and row statistics locally -- one exchange per block.
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;   // query head
-    const int own_lo = rank == 0 ? 0 : 64;  // rows whose softmax this rank owns
-    const bool owner = row >= own_lo && row < own_lo + 64;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    float *alpha = reinterpret_cast<float *>(smem + kOffAlpha);
-    float *stats = reinterpret_cast<float *>(smem + kOffStats);
     const float *sx = reinterpret_cast<const float *>(smem + kOffSx);
     long long g = 0;
-    int segn = 0, pairn = 0;
+    int pairn = 0;
     bool ok = true;
     for (int si = seg_lo; si < seg_hi; ++si) {
       const int4 sg = segs[si];
@@ -436,28 +449,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float mref = -INFINITY, l = 0.f, lf = 0.f;
       for (int j = 0; j < nb; ++j, ++g) {
         const int w0 = (tb / kBlk) * kBlk + j * kBlk;
-        const int sb = int(g & 1);
+        const int sb = int(g & 1), pb = int(g & 1);
         float s[64];
+        long long t0 = clock64();
         ok = ok && cx.wait(sb ? B_SF1 : B_SF0, uint32_t((g >> 1) & 1));
+        tw(2, t0);
+        if (tr && threadIdx.x == 64) atomicAdd(reinterpret_cast<unsigned long long *>(tr + 13), 1ull);
         tc_fence_after();
         tmem_ld32(tS[sb] + lane_off, s);
         tmem_ld32(tS[sb] + lane_off + 32, s + 32);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(cx.bar(sb ? B_SE1 : B_SE0));
-        if (!owner) {
-          // send this partial to the rank that owns the row
-          ok = ok && cx.wait(B_SXFREE, uint32_t((g & 1) ^ 1));
-          const uint32_t dst = cx.peer_addr(cx.sbase + kOffSx + uint32_t((row - (64 - own_lo)) * 64 * 4));
+        // ---- exchange partial scores with the partner ----
+        t0 = clock64();
+        ok = ok && cx.wait(B_SXFREE, uint32_t((g & 1) ^ 1));
+        const uint32_t dst = cx.peer_addr(cx.sbase + kOffSx + uint32_t(row) * 256);
 #pragma unroll
-          for (int c = 0; c < 64; c += 4)
-            st_cluster_v4(dst + c * 4, __float_as_uint(s[c]), __float_as_uint(s[c + 1]),
-                          __float_as_uint(s[c + 2]), __float_as_uint(s[c + 3]));
-          __syncwarp();
-          if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_SXF)));
-        } else {
-          ok = ok && cx.wait(B_SXF, uint32_t(g & 1));
-          const float *mine = sx + (row - own_lo) * 64;
+        for (int c = 0; c < 64; c += 4)
+          st_cluster_v4(dst + c * 4, __float_as_uint(s[c]), __float_as_uint(s[c + 1]), __float_as_uint(s[c + 2]),
+                        __float_as_uint(s[c + 3]));
+        __syncwarp();
+        if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_SXF)));
+        ok = ok && cx.wait(B_SXF, uint32_t(g & 1));
+        tw(3, t0);
+        {
+          const float *mine = sx + row * 64;
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
             const float4 v = *reinterpret_cast<const float4 *>(mine + c);
@@ -466,69 +483,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             s[c + 2] += v.z;
             s[c + 3] += v.w;
           }
-          __syncwarp();
-          if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_SXFREE)));
-          // ---- online softmax of this row (thread-local) ----
-          float mx = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int tok = w0 + c;
-            s[c] = (tok >= tb && tok < te) ? s[c] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, s[c]);
-          }
-          float a = 1.f;
-          if (j == 0) {
-            mref = mx;
-          } else if (mx > mref + kTau) {
-            a = exp2f(mref - mx);
-            mref = mx;
-            l *= a;
-            lf *= a;
-          }
-          uint32_t pk[32];
-          float ps = 0.f, pf = 0.f;
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float e0 = exp2f(s[c] - mref), e1 = exp2f(s[c + 1] - mref);
-            pf += e0 + e1;
-            pk[c / 2] = ptx::pack_bf16(e0, e1);
-            const float2 f = ptx::unpack_bf16(pk[c / 2]);
-            ps += f.x + f.y;
-          }
-          l += ps;
-          lf += pf;
-          // P rows go into both ranks' P buffers once both PVs of the previous block are done
-          ok = ok && cx.wait(B_PVD, uint32_t((g & 1) ^ 1));
-          const uint32_t prow = cx.sbase + kOffP + uint32_t(row) * 128;
-          const uint32_t prow_peer = cx.peer_addr(prow);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t o = uint32_t((c ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + o), "r"(pk[4 * c]),
-                         "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                         : "memory");
-            st_cluster_v4(prow_peer + o, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          }
-          alpha[row] = a;
-          st_cluster_f32(cx.peer_addr(cx.sbase + kOffAlpha + 4u * row), a);
-          fence_proxy_async_all();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(cx.bar(B_PF));
-            arrive_remote(cx.peer_addr(cx.bar(B_PF)));
-          }
         }
-        // ---- every row: rescale this rank's O columns if the owner moved the max ----
-        ok = ok && cx.wait(B_PF, uint32_t(g & 1));
-        ok = ok && cx.wait(B_PVD, uint32_t((g & 1) ^ 1));  // previous PV done: O stable
-        tc_fence_after();
-        const float ar = alpha[row];
-        if (j > 0 && __any_sync(0xffffffffu, ar != 1.f)) {
+        __syncwarp();
+        if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_SXFREE)));
+        // ---- online softmax of this row (thread-local) ----
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int tok = w0 + c;
+          s[c] = (tok >= tb && tok < te) ? s[c] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+        float a = 1.f;
+        if (j == 0) {
+          mref = mx;
+        } else if (mx > mref + kTau) {
+          a = exp2f(mref - mx);
+          mref = mx;
+          l *= a;
+          lf *= a;
+        }
+        uint32_t pk[32];
+        float ps = 0.f, pf = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float e0 = exp2f(s[c] - mref), e1 = exp2f(s[c + 1] - mref);
+          pf += e0 + e1;
+          pk[c / 2] = ptx::pack_bf16(e0, e1);
+          const float2 f = ptx::unpack_bf16(pk[c / 2]);
+          ps += f.x + f.y;
+        }
+        l += ps;
+        lf += pf;
+        // P row into P buffer pb once PV(g-2), its previous reader, is done
+        t0 = clock64();
+        ok = ok && cx.wait(B_PVD0 + pb, uint32_t(((g >> 1) & 1) ^ 1));
+        tw(4, t0);
+        {
+          const uint32_t prow = cx.sbase + kOffP + uint32_t(pb) * 16384 + uint32_t(row) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + uint32_t((c ^ (row & 7)) << 4)),
+                         "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                         : "memory");
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(cx.bar(B_PF0 + pb));
+        // ---- rescale this rank's O columns if the max moved (rare) ----
+        // (MMAs from one thread run in order, so without a rescale PV(g) may
+        // follow PV(g-1) at once; a rescale first waits for PV(g-1) to finish)
+        if (j > 0 && __any_sync(0xffffffffu, a != 1.f)) {
+          t0 = clock64();
+          ok = ok && cx.wait(B_PVD0 + int((g - 1) & 1), uint32_t(((g - 1) >> 1) & 1));
+          tw(5, t0);
+          tc_fence_after();
           float v[32];
           for (int c = 0; c < 256; c += 32) {
             tmem_ld32(tO + lane_off + c, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= ar;
+            for (int i = 0; i < 32; ++i) v[i] *= a;
             tmem_st32(tO + lane_off + c, v);
           }
         }
@@ -548,29 +562,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(cx.bar(B_OR));
+        if (lane == 0) ptx::mbar_arrive(cx.bar(B_OR0 + pb));
       }
-      // ---- segment end: wait for the last PV, exchange row statistics ----
-      ok = ok && cx.wait(B_PVD, uint32_t((g - 1) & 1));
+      // ---- segment end: wait for the last PV; this thread holds its row's stats ----
+      ok = ok && cx.wait(B_PVD0 + int((g - 1) & 1), uint32_t(((g - 1) >> 1) & 1));
       tc_fence_after();
-      if (owner) {
-        stats[row] = mref;
-        stats[128 + row] = l;
-        stats[256 + row] = lf;
-        st_cluster_f32(cx.peer_addr(cx.sbase + kOffStats + 4u * row), mref);
-        st_cluster_f32(cx.peer_addr(cx.sbase + kOffStats + 4u * (128 + row)), l);
-        st_cluster_f32(cx.peer_addr(cx.sbase + kOffStats + 4u * (256 + row)), lf);
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(cx.bar(B_STF));
-          arrive_remote(cx.peer_addr(cx.bar(B_STF)));
-        }
-      }
-      ok = ok && cx.wait(B_STF, uint32_t(segn & 1));
-      ++segn;
-      const float rm = stats[row], rl = stats[128 + row], rlf = stats[256 + row];
       if (wslot < 0) {
-        const float inv = 1.f / rl;
+        const float inv = 1.f / l;
         float v[32];
         for (int c = 0; c < 256; c += 32) {
           tmem_ld32(tO + lane_off + c, v);
@@ -581,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
-        if (rank == 0) p.lse[orow] = (rm + log2f(rlf)) * kLn2;
+        if (rank == 0) p.lse[orow] = (mref + log2f(lf)) * kLn2;
       } else {
         float *ps = p.partials + int64_t(wslot) * p.slot_floats;
         float v[32];
@@ -592,9 +590,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         if (rank == 0) {
-          ps[kHeads * kDv + row] = rm;
-          ps[kHeads * kDv + kHeads + row] = rl;
-          ps[kHeads * kDv + 2 * kHeads + row] = rlf;
+          ps[kHeads * kDv + row] = mref;
+          ps[kHeads * kDv + kHeads + row] = l;
+          ps[kHeads * kDv + 2 * kHeads + row] = lf;
         }
       }
       tc_fence_before();
@@ -675,8 +673,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u));
   }
+  if (tr && lane == 0) {
+    const int slot = warp == 0 ? 12 : (warp == 1 ? 11 : 10);
+    atomicAdd(reinterpret_cast<unsigned long long *>(tr + slot), (unsigned long long)(clock64() - tk0));
+  }
   if (tr && threadIdx.x == 0) {
-    tr[6] = seg_hi - seg_lo;
+    tr[14] = seg_hi - seg_lo;
+    tr[15] = ptx::smid();
     tr[1] = (long long)ptx::globaltimer_ns();
   }
 }
@@ -719,7 +722,7 @@ int launch_mla(const DecodeArgs &a) {
   p.max_slots = int(a.wl.slots);
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.slot_floats = a.wl.slot_floats;
-  p.trace = static_cast<long long *>(trace_buffer(a.n_ctas));
+  p.trace = static_cast<long long *>(trace_buffer(2 * a.n_ctas));
   // stages per rank: shared memory = fixed region + Q + stages (both ranks get the same size)
   const int budget = 227 * 1024 - 1024;
   p.nst0 = std::min(kMaxSt, (budget - kOffQ - 4 * kHeads * 128) / (4 * kBlk * 128));
