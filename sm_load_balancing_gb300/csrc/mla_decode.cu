@@ -10,20 +10,20 @@
 // observation that a cluster of SMs can cooperate through TMA/mbarrier is what
 // the pair below uses).
 //
-// One worker = a 2-CTA cluster. TMEM holds 128 lanes x 512 fp32 columns: one
-// 128x512 output accumulator, with no room for scores, and Q alone is 147 KB of
-// shared memory, so the contraction is split over the pair:
-//   rank 0 streams latent columns [0, 256), rank 1 columns [256, 576), one TMA
-//   box per 64-token block each (no byte is read twice);
-//   S = Q K^T: each rank computes the partial sum over its own columns
-//   (M=128 heads, N=64 tokens) into TMEM and sends it to the partner over
-//   DSMEM; both ranks add the two partials (same bits: addition commutes) and
-//   run the same online softmax, one thread per head row;
-//   O = P V: each rank accumulates its 256 value columns for all 128 heads in
-//   TMEM (M=128, N=256, K=64 tokens) from its own copy of P.
-// The running maximum is kept per row and only moved (with an O rescale) when
-// a block's maximum exceeds it by more than 2^8, so p <= 256 and rescales are
-// rare; l and O stay consistent with the same reference maximum.
+// One worker = a 2-CTA cluster with a producer/consumer split of the math.
+// TMEM holds 128 lanes x 512 fp32 columns per SM, and the 128x512 fp32 output
+// accumulator alone fills it, so the two contractions live on different SMs:
+//   rank 0 (scores): Q [128 heads][576] sits in its TMEM as the A operand
+//     (loaded once per segment), S = Q K^T runs with M=128 heads, N=64 tokens,
+//     K=576 per 64-token block into a double-buffered TMEM score tile, and its
+//     epilogue warps run the online softmax (one thread per head row) and
+//     write the bf16 probabilities P straight into rank 1's shared memory;
+//   rank 1 (values): O += P V with M=128, N=2x256, K=64 into its TMEM.
+// Each 64-token block is read from HBM once: one TMA box with the 512 value
+// columns is multicast into both CTAs, the 64 rope columns go to rank 0 only.
+// The running maximum is kept per row and only moved (with an O rescale on
+// rank 1) when a block's maximum exceeds it by more than 2^8, so p <= 256 and
+// rescales are rare; l and O stay consistent with the same reference maximum.
 // Every wait is bounded; a timeout sets the error word and an abort flag in
 // both ranks so that the pair drains quickly.
 #include <math.h>
@@ -38,29 +38,54 @@ namespace skd {
 namespace {
 
 constexpr int kHeads = 128, kDk = 576, kDv = 512, kBlk = 64;
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kMaxSt = 4;
-constexpr float kTau = 8.f;  // lazy-rescale threshold, log2 units
+constexpr int kThreads = 192;  // warp 0 TMA (rank 0), warp 1 MMA, warps 2-5 epilogue
+constexpr int kNst = 3;        // KV ring stages
+constexpr float kTau = 8.f;    // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kTraceWords = SKD_TRACE_RECORD_BYTES / 8;
 
-// fixed shared-memory region (same offsets in both ranks, for DSMEM)
-constexpr int kOffP = 0;                     // P [2 buffers][128 rows][64 tok] bf16, SW128: 32 KB
-constexpr int kOffSx = 32768;                // partner's partial scores [128][64] fp32: 32 KB
-constexpr int kOffBar = 65536;               // mbarriers
-constexpr int kNumBar = 2 * kMaxSt + 20;
-constexpr int kOffMisc = kOffBar + kNumBar * 8;  // tmem base, flags
-constexpr int kOffQ = 65 * 1024;             // Q [nch][128][128 B], then KV stages
+// shared memory (offsets are the same in both ranks: TMA multicast and DSMEM
+// stores address the partner's buffers by the local offset)
+constexpr uint32_t kChunkBytes = kBlk * 128;       // 64 columns x 64 tokens, bf16, SW128
+constexpr uint32_t kMainBytes = 8 * kChunkBytes;   // value columns [0, 512) of one block
+constexpr uint32_t kOffRing = 0;                   // [kNst][64 KB], both ranks
+constexpr uint32_t kOffRope = kNst * kMainBytes;   // rank 0: [kNst][8 KB] columns [512, 576)
+constexpr uint32_t kOffP = kNst * kMainBytes;      // rank 1: P [2][128 rows][64 tok] bf16, SW128
+constexpr uint32_t kPBytes = kHeads * kBlk * 2;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;  // mbarriers
+constexpr int kNumBar = 24;
+constexpr uint32_t kOffA = kOffBar + kNumBar * 8;  // rank 1: rescale factors [2][128] fp32
+constexpr uint32_t kOffStats = kOffA + 2 * kHeads * 4;  // rank 1: m, l, lf [3][128] fp32
+constexpr uint32_t kOffMisc = kOffStats + 3 * kHeads * 4;
+// misc words: 0 tmem base, 1 abort, 2 merge decision, 3 blocks issued by the
+// producer, 4..11 rescale flags [P buffer][quarter]
+constexpr uint32_t kSmemBytes = kOffMisc + 64;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kOffRope + kNst * kChunkBytes <= kOffBar, "rope ring overlaps the barriers");
 
-// barrier indices
-// (P buffers alternate per block; B_PF*, B_PVD* and B_OR* come in pairs, one per
-// buffer, so that no barrier can run two phases ahead of a waiter)
+// TMEM columns
+constexpr uint32_t kTQ = 0;                     // rank 0: Q, 288 columns (2 bf16 per column)
+constexpr uint32_t kTS0 = 384, kTS1 = 448;      // rank 0: score tiles, 64 columns each
+constexpr uint32_t kTO = 0;                     // rank 1: O, 512 columns
+
 enum {
-  B_KVF = 0, B_KVE = kMaxSt, B_QF = 2 * kMaxSt, B_QE, B_SF0, B_SF1, B_SE0, B_SE1, B_SXF, B_SXFREE,
-  B_PF0, B_PF1, B_PVD0, B_PVD1, B_OR0, B_OR1, B_STF, B_PAIR, B_GO, B_FIN
+  B_KVF = 0,            // [kNst] block landed (rank 0: 72 KB, rank 1: 64 KB)
+  B_KVE = kNst,         // [kNst] rank 0: stage free (rank 0 QK done + rank 1 PV done)
+  B_QF = 2 * kNst,      // rank 0: Q of the segment is in TMEM (4 epilogue warps)
+  B_SF0, B_SF1,         // rank 0: score tile complete
+  B_SE0, B_SE1,         // rank 0: score tile read out (4)
+  B_PF0, B_PF1,         // rank 1: P, factors and flags of the block landed (4 remote)
+  B_PVD0, B_PVD1,       // both: PV of the block that used P buffer 0/1 complete
+  B_OR0, B_OR1,         // rank 1: O rescaled / V tail zeroed, PV may run (4)
+  B_STF,                // rank 1: segment statistics landed (4 remote)
+  B_STE,                // rank 0: statistics buffer free (4 remote)
+  B_FIN,                // MMA drain before TMEM release
+  B_COUNT
 };
+static_assert(B_COUNT <= kNumBar, "barrier count");
 
 struct Params {
+  const __nv_bfloat16 *q;
   const int32_t *page_table;
   const int32_t *seqlens;
   const int32_t *plan;
@@ -69,7 +94,7 @@ struct Params {
   float *partials;
   __nv_bfloat16 *out;
   float *lse;
-  int batch, P, max_pages, num_pages, max_slots, nst0, nst1;
+  int batch, P, max_pages, num_pages, max_slots;
   float scale_log2;
   int64_t slot_floats;
   long long *trace;
@@ -99,6 +124,11 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+__device__ __forceinline__ void arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -112,6 +142,11 @@ __device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) 
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -127,23 +162,33 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+// D (TMEM) (+)= A (shared memory) * B (shared memory)
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
           d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(acc)
       : "memory");
 }
+// D (TMEM) (+)= A (TMEM: lane = row, column c = elements 2c, 2c+1) * B (shared memory)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// arrive on the barrier at the same offset in every CTA of `mask`
 __device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
 }
-// 32 lanes x 32 consecutive fp32 columns per warp (lane = TMEM lane of the warp's quarter)
+// 32 lanes x 32 consecutive 32-bit columns per warp (lane = TMEM lane of the warp's quarter)
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
   asm volatile(
@@ -159,14 +204,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
-      "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
-      "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
-      "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -179,9 +224,17 @@ __device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap *m, uint32_
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
       : "memory");
 }
+// same box into every CTA of `mask` (same offset; each CTA's barrier at `bar`'s offset counts its bytes)
+__device__ __forceinline__ void tma3_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2,
+                                        uint16_t mask, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::"
+      "cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask), "l"(pol)
+      : "memory");
+}
 
 struct Ctx {
-  uint8_t *smem;
   uint32_t sbase, peer;  // own shared base; peer rank
   volatile int *abort;
   int32_t *err;
@@ -208,13 +261,13 @@ struct Ctx {
   }
 };
 
+// number of 64-token blocks touched by the token range [tb, te)
+__device__ __forceinline__ int num_blocks(int tb, int te) { return (te + kBlk - 1) / kBlk - tb / kBlk; }
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tq0, const __grid_constant__ CUtensorMap tq1,
-                      const __grid_constant__ CUtensorMap tkv0, const __grid_constant__ CUtensorMap tkv1,
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmain, const __grid_constant__ CUtensorMap trope,
                       const Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int worker = blockIdx.x >> 1;
@@ -226,79 +279,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicOr(p.err, plan[PH_ERR] != 0 ? plan[PH_ERR] : SKD_DEVERR_PLAN);
     return;  // both ranks take this path alike
   }
+  Ctx cx;
+  cx.sbase = ptx::smem_u32(smem);
+  // the 128-byte swizzle needs 1024-byte aligned tiles; the dynamic window
+  // starts aligned when the kernel declares no static shared memory
+  if (cx.sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, SKD_DEVERR_PLAN);
+    return;  // same offset in both ranks
+  }
   const PlanOffsets off = plan_offsets(p.batch, 1, nworkers);
   const int seg_lo = plan[off.cta_off + worker], seg_hi = plan[off.cta_off + worker + 1];
   const int4 *segs = reinterpret_cast<const int4 *>(plan + off.segs);
 
-  const int nch = rank == 0 ? 4 : 5;              // 64-column chunks this rank streams
-  const int chunk0 = rank == 0 ? 0 : 4;
-  const int nst = rank == 0 ? p.nst0 : p.nst1;
-  const uint32_t stage_bytes = uint32_t(nch) * kBlk * 128;
-  const uint32_t q_bytes = uint32_t(nch) * kHeads * 128;
-  const CUtensorMap *tq = rank == 0 ? &tq0 : &tq1;
-  const CUtensorMap *tkv = rank == 0 ? &tkv0 : &tkv1;
-
-  Ctx cx;
-  cx.smem = smem;
-  cx.sbase = ptx::smem_u32(smem);
   cx.peer = rank ^ 1u;
   cx.abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
   cx.err = p.err;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
-  const uint32_t sQ = cx.sbase + kOffQ;
-  const uint32_t sKV = sQ + q_bytes;
+  volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < nst; ++s) {
+    for (int s = 0; s < kNst; ++s) {
       ptx::mbar_init(cx.bar(B_KVF + s), 1);
-      ptx::mbar_init(cx.bar(B_KVE + s), 1);
+      ptx::mbar_init(cx.bar(B_KVE + s), 2);
     }
-    ptx::mbar_init(cx.bar(B_QF), 1);
-    ptx::mbar_init(cx.bar(B_QE), 1);
+    ptx::mbar_init(cx.bar(B_QF), 4);
     ptx::mbar_init(cx.bar(B_SF0), 1);
     ptx::mbar_init(cx.bar(B_SF1), 1);
     ptx::mbar_init(cx.bar(B_SE0), 4);
     ptx::mbar_init(cx.bar(B_SE1), 4);
-    ptx::mbar_init(cx.bar(B_SXF), 4);
-    ptx::mbar_init(cx.bar(B_SXFREE), 4);
     ptx::mbar_init(cx.bar(B_PF0), 4);
     ptx::mbar_init(cx.bar(B_PF1), 4);
     ptx::mbar_init(cx.bar(B_PVD0), 1);
     ptx::mbar_init(cx.bar(B_PVD1), 1);
     ptx::mbar_init(cx.bar(B_OR0), 4);
     ptx::mbar_init(cx.bar(B_OR1), 4);
-    ptx::mbar_init(cx.bar(B_PAIR), 1);
-    ptx::mbar_init(cx.bar(B_GO), 1);
+    ptx::mbar_init(cx.bar(B_STF), 4);
+    ptx::mbar_init(cx.bar(B_STE), 4);
     ptx::mbar_init(cx.bar(B_FIN), 1);
-    *cx.abort = 0;
+    misc[1] = 0;
+    misc[3] = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     cx.sbase + kOffMisc),
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(cx.sbase + kOffMisc),
                  "r"(512u));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   cluster_sync();  // barriers of both ranks initialised before any remote arrive
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tS[2] = {tmem + 0, tmem + 64};  // partial / full scores, double buffered
-  const uint32_t tO = tmem + 128;                 // this rank's 256 value columns
+  const uint32_t tmem = misc[0];
 
-  // trace (when enabled): one record per CTA; words 2.. accumulate wait cycles
   long long *const tr = p.trace ? p.trace + int64_t(blockIdx.x) * kTraceWords : nullptr;
   if (tr && threadIdx.x == 0) tr[0] = (long long)ptx::globaltimer_ns();
-  auto tw = [&](int idx, long long t0) {
-    if (tr && lane == 0) atomicAdd(reinterpret_cast<unsigned long long *>(tr + idx), (unsigned long long)(clock64() - t0));
-  };
-  const long long tk0 = clock64();
 
-  if (warp == 0) {
+  const int q4 = warp & 3;                       // TMEM lane quarter of an epilogue warp
+  const int row = q4 * 32 + lane;                // query head of an epilogue thread
+  const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+
+  if (rank == 0 && warp == 0) {
     // ============================ TMA producer ===============================
     const uint64_t pol = ptx::policy_evict_first();
-    int st = 0, qn = 0;
-    uint32_t ph = 0;
+    int g = 0;
     bool ok = true;
     for (int si = seg_lo; si < seg_hi && ok; ++si) {
       const int4 sg = segs[si];
@@ -308,16 +349,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const int L = p.seqlens[b];
         if (te > L || L > p.max_pages * p.P) atomicOr(p.err, SKD_DEVERR_SEQLEN);
-        ok = cx.wait(B_QE, (qn & 1) ^ 1u);
-        if (ok) {
-          ptx::mbar_arrive_expect_tx(cx.bar(B_QF), q_bytes);
-          tma3(sQ, tq, cx.bar(B_QF), 0, b * kHeads, chunk0, pol);
-        }
       }
-      ++qn;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      const int w_lo = (tb / kBlk) * kBlk;
-      for (int w0 = w_lo; w0 < te && ok; w0 += kBlk) {
+      for (int w0 = (tb / kBlk) * kBlk; w0 < te && ok; w0 += kBlk, ++g) {
+        const int s = g % kNst;
+        const uint32_t ph = uint32_t(g / kNst) & 1u;
         if (lane == 0) {
           const int j = w0 / p.P;
           int pg = j < p.max_pages ? __ldg(ptab + j) : -1;
@@ -325,168 +360,126 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             atomicOr(p.err, SKD_DEVERR_PAGE);
             pg = 0;
           }
-          const long long t0 = clock64();
-          ok = cx.wait(B_KVE + st, ph ^ 1u);
-          tw(9, t0);
+          ok = cx.wait(B_KVE + s, ph ^ 1u);
           if (ok) {
-            ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + st), stage_bytes);
-            tma3(sKV + st * stage_bytes, tkv, cx.bar(B_KVF + st), 0, pg * p.P + (w0 % p.P), chunk0, pol);
+            const int rowk = pg * p.P + (w0 % p.P);
+            ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), kMainBytes + kChunkBytes);
+            arrive_expect_tx_remote(cx.peer_addr(cx.bar(B_KVF + s)), kMainBytes);
+            tma3_mc(cx.sbase + kOffRing + s * kMainBytes, &tmain, cx.bar(B_KVF + s), 0, rowk, 0, 0x3, pol);
+            tma3(cx.sbase + kOffRope + s * kChunkBytes, &trope, cx.bar(B_KVF + s), 0, rowk, 8, pol);
+            misc[3] = uint32_t(g + 1);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (++st == nst) {
-          st = 0;
-          ph ^= 1u;
-        }
       }
     }
+    if (lane == 0) st_cluster_u32(cx.peer_addr(cx.sbase + kOffMisc + 12), misc[3]);
   } else if (warp == 1) {
     // ============================ MMA issuer =================================
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc(kHeads, kBlk, 0);
-      constexpr uint32_t id_pv = idesc(kHeads, 256, 1);
-      int st = 0, qn = 0;
-      uint32_t ph = 0;
-      long long g = 0;  // global block counter (S buffers and per-block barriers)
+      int g = 0, qn = 0;
       bool ok = true;
-      for (int si = seg_lo; si < seg_hi && ok; ++si) {
-        const int4 sg = segs[si];
-        const int tb = sg.y, te = sg.z;
-        if (te <= tb) continue;
-        const int nb = (te + kBlk - 1) / kBlk - tb / kBlk;
-        ok = cx.wait(B_QF, qn & 1);
-        ++qn;
-        tc_fence_after();
-        auto issue_qk = [&](long long gg, int stage) {
-          const int sb = int(gg & 1);
-          const long long t0 = clock64();
-          if (!cx.wait(sb ? B_SE1 : B_SE0, uint32_t(((gg >> 1) & 1) ^ 1))) return false;
-          tw(8, t0);
+      if (rank == 0) {
+        constexpr uint32_t id_qk = idesc(kHeads, kBlk, 0);
+        for (int si = seg_lo; si < seg_hi && ok; ++si) {
+          const int4 sg = segs[si];
+          if (sg.z <= sg.y) continue;
+          const int nb = num_blocks(sg.y, sg.z);
+          ok = cx.wait(B_QF, uint32_t(qn & 1));
+          ++qn;
           tc_fence_after();
-          for (int c = 0; c < nch; ++c)
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = sdesc(sQ + c * (kHeads * 128) + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc(sKV + stage * stage_bytes + c * (kBlk * 128) + kk * 32, 16, 1024);
-              umma(tS[sb], a, bd, id_qk, (c | kk) != 0);
+          for (int j = 0; j < nb && ok; ++j, ++g) {
+            const int s = g % kNst, sb = g & 1;
+            if (!cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u) || !cx.wait(B_SE0 + sb, uint32_t((g >> 1) & 1) ^ 1u)) {
+              ok = false;
+              break;
             }
-          umma_commit(cx.bar(sb ? B_SF1 : B_SF0));
-          return true;
-        };
-        // block 0 of the segment
-        int st_j = st;
-        uint32_t ph_j = ph;
-        ok = ok && cx.wait(B_KVF + st_j, ph_j);
-        ok = ok && issue_qk(g, st_j);
-        for (int j = 0; j < nb && ok; ++j) {
-          // issue QK of block j+1 before waiting for the softmax of block j
-          int st_n = st_j + 1;
-          uint32_t ph_n = ph_j;
-          if (st_n == nst) {
-            st_n = 0;
-            ph_n ^= 1u;
+            tc_fence_after();
+            const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
+            const uint32_t rope = cx.sbase + kOffRope + s * kChunkBytes;
+            const uint32_t dS = tmem + (sb ? kTS1 : kTS0);
+#pragma unroll
+            for (int c = 0; c < 9; ++c) {
+              const uint32_t bc = c < 8 ? ring + c * kChunkBytes : rope;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ts(dS, tmem + kTQ + c * 32 + kk * 8, sdesc(bc + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
+            }
+            umma_commit(cx.bar(B_SF0 + sb));
+            umma_commit(cx.bar(B_KVE + s));
           }
-          if (j + 1 < nb) {
-            const long long t0 = clock64();
-            ok = cx.wait(B_KVF + st_n, ph_n);
-            tw(6, t0);
-            ok = ok && issue_qk(g + 1, st_n);
-            if (!ok) break;
-          } else {
-            umma_commit(cx.bar(B_QE));  // Q is free once this segment's last QK completes
-          }
-          // PV of block j (P buffer g & 1)
-          const int pb = int(g & 1);
-          const long long t0 = clock64();
-          if (!cx.wait(B_PF0 + pb, uint32_t((g >> 1) & 1)) || !cx.wait(B_OR0 + pb, uint32_t((g >> 1) & 1))) {
-            ok = false;
-            break;
-          }
-          tw(7, t0);
-          tc_fence_after();
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = sdesc(cx.sbase + kOffP + pb * 16384 + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc(sKV + st_j * stage_bytes + kk * (16 * 128), kBlk * 128, 1024);
-            umma(tO, a, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(cx.bar(B_KVE + st_j));
-          umma_commit(cx.bar(B_PVD0 + pb));
-          st_j = st_n;
-          ph_j = ph_n;
-          ++g;
         }
-        st = st_j;
-        ph = ph_j;
+      } else {
+        constexpr uint32_t id_pv = idesc(kHeads, 256, 1);
+        for (int si = seg_lo; si < seg_hi && ok; ++si) {
+          const int4 sg = segs[si];
+          if (sg.z <= sg.y) continue;
+          const int nb = num_blocks(sg.y, sg.z);
+          for (int j = 0; j < nb; ++j, ++g) {
+            const int s = g % kNst, pb = g & 1;
+            if (!cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u) || !cx.wait(B_OR0 + pb, uint32_t((g >> 1) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
+            const uint32_t pbuf = cx.sbase + kOffP + pb * kPBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = sdesc(pbuf + kk * 32, 16, 1024);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                umma_ss(tmem + kTO + h * 256, a, sdesc(ring + h * 4 * kChunkBytes + kk * (16 * 128), 8192, 1024),
+                        id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit_mc(cx.bar(B_KVE + s), 0x1);   // rank 0 owns the ring
+            umma_commit_mc(cx.bar(B_PVD0 + pb), 0x3);  // P buffer free (rank 0), O ready (rank 1)
+          }
+        }
       }
       // every MMA this thread issued has completed before TMEM is released
       umma_commit(cx.bar(B_FIN));
-      cx.wait(B_FIN, 0);
+      ptx::mbar_wait(cx.bar(B_FIN), 0, nullptr, kWaitCycles);
     }
-  } else {
-    // ============================ epilogue warps =============================
-    // Each rank computes the softmax of all 128 rows: it sends its partial
-    // scores to the partner and adds the partner's, so both ranks hold the same
-    // full scores (fp32 addition commutes) and derive the same P, rescale
-    // factors and row statistics locally -- one exchange per block.
-    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + lane;   // query head
-    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const float *sx = reinterpret_cast<const float *>(smem + kOffSx);
-    long long g = 0;
-    int pairn = 0;
+  } else if (rank == 0 && warp >= 2) {
+    // ====================== rank 0 epilogue: online softmax ====================
+    int g = 0, stn = 0;
     bool ok = true;
     for (int si = seg_lo; si < seg_hi; ++si) {
       const int4 sg = segs[si];
-      const int b = sg.x, tb = sg.y, te = sg.z, wslot = sg.w;
-      const int64_t orow = int64_t(b) * kHeads + row;
-      if (te <= tb) {  // empty request
-        uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256);
-        for (int c = 0; c < 32; ++c) o4[c] = make_uint4(0, 0, 0, 0);
-        if (rank == 0) p.lse[orow] = -INFINITY;
-        continue;
+      const int b = sg.x, tb = sg.y, te = sg.z;
+      if (te <= tb) continue;
+      const int nb = num_blocks(tb, te);
+      // Q row of this head into TMEM (the previous segment's score MMAs have
+      // completed: this thread saw the score tile of its last block)
+      {
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q) + (int64_t(b) * kHeads + row) * (kDk / 8);
+#pragma unroll 1
+        for (int c = 0; c < 9; c += 3) {
+          uint4 v[24];
+#pragma unroll
+          for (int i = 0; i < 24; ++i) v[i] = __ldg(qrow + c * 8 + i);
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc)
+            tmem_st32(tmem + kTQ + lane_off + (c + cc) * 32, reinterpret_cast<const uint32_t *>(v + cc * 8));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(cx.bar(B_QF));
       }
-      const int L = p.seqlens[b];
-      const int nb = (te + kBlk - 1) / kBlk - tb / kBlk;
       float mref = -INFINITY, l = 0.f, lf = 0.f;
       for (int j = 0; j < nb; ++j, ++g) {
         const int w0 = (tb / kBlk) * kBlk + j * kBlk;
-        const int sb = int(g & 1), pb = int(g & 1);
+        const int sb = g & 1, pb = g & 1;
         float s[64];
-        long long t0 = clock64();
-        ok = ok && cx.wait(sb ? B_SF1 : B_SF0, uint32_t((g >> 1) & 1));
-        tw(2, t0);
-        if (tr && threadIdx.x == 64) atomicAdd(reinterpret_cast<unsigned long long *>(tr + 13), 1ull);
+        ok = ok && cx.wait(B_SF0 + sb, uint32_t((g >> 1) & 1));
         tc_fence_after();
-        tmem_ld32(tS[sb] + lane_off, s);
-        tmem_ld32(tS[sb] + lane_off + 32, s + 32);
+        const uint32_t tS = tmem + (sb ? kTS1 : kTS0) + lane_off;
+        tmem_ld32(tS, s);
+        tmem_ld32(tS + 32, s + 32);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(cx.bar(sb ? B_SE1 : B_SE0));
-        // ---- exchange partial scores with the partner ----
-        t0 = clock64();
-        ok = ok && cx.wait(B_SXFREE, uint32_t((g & 1) ^ 1));
-        const uint32_t dst = cx.peer_addr(cx.sbase + kOffSx + uint32_t(row) * 256);
-#pragma unroll
-        for (int c = 0; c < 64; c += 4)
-          st_cluster_v4(dst + c * 4, __float_as_uint(s[c]), __float_as_uint(s[c + 1]), __float_as_uint(s[c + 2]),
-                        __float_as_uint(s[c + 3]));
-        __syncwarp();
-        if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_SXF)));
-        ok = ok && cx.wait(B_SXF, uint32_t(g & 1));
-        tw(3, t0);
-        {
-          const float *mine = sx + row * 64;
-#pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(mine + c);
-            s[c] += v.x;
-            s[c + 1] += v.y;
-            s[c + 2] += v.z;
-            s[c + 3] += v.w;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_SXFREE)));
-        // ---- online softmax of this row (thread-local) ----
+        if (lane == 0) ptx::mbar_arrive(cx.bar(B_SE0 + sb));
         float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
@@ -515,153 +508,216 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         l += ps;
         lf += pf;
-        // P row into P buffer pb once PV(g-2), its previous reader, is done
-        t0 = clock64();
+        // P row into rank 1's buffer pb once PV(g-2), its previous reader, is done
         ok = ok && cx.wait(B_PVD0 + pb, uint32_t(((g >> 1) & 1) ^ 1));
-        tw(4, t0);
         {
-          const uint32_t prow = cx.sbase + kOffP + uint32_t(pb) * 16384 + uint32_t(row) * 128;
+          const uint32_t prow = cx.peer_addr(cx.sbase + kOffP + uint32_t(pb) * kPBytes + uint32_t(row) * 128);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + uint32_t((c ^ (row & 7)) << 4)),
-                         "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                         : "memory");
+            st_cluster_v4(prow + uint32_t((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                          pk[4 * c + 3]);
+          st_cluster_f32(cx.peer_addr(cx.sbase + kOffA + uint32_t(pb * kHeads + row) * 4), a);
+          const uint32_t any = __any_sync(0xffffffffu, a != 1.f) ? 1u : 0u;
+          if (lane == 0) st_cluster_u32(cx.peer_addr(cx.sbase + kOffMisc + 16 + uint32_t(pb * 4 + q4) * 4), any);
         }
-        ptx::fence_proxy_async_smem();
+        fence_proxy_async_all();  // P is read by rank 1's tensor core (async proxy)
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(cx.bar(B_PF0 + pb));
-        // ---- rescale this rank's O columns if the max moved (rare) ----
-        // (MMAs from one thread run in order, so without a rescale PV(g) may
-        // follow PV(g-1) at once; a rescale first waits for PV(g-1) to finish)
-        if (j > 0 && __any_sync(0xffffffffu, a != 1.f)) {
-          t0 = clock64();
-          ok = ok && cx.wait(B_PVD0 + int((g - 1) & 1), uint32_t(((g - 1) >> 1) & 1));
-          tw(5, t0);
+        if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_PF0 + pb)));
+      }
+      // segment end: row statistics to rank 1
+      ok = ok && cx.wait(B_STE, uint32_t(stn & 1) ^ 1u);
+      const uint32_t st = cx.peer_addr(cx.sbase + kOffStats + uint32_t(row) * 4);
+      st_cluster_f32(st, mref);
+      st_cluster_f32(st + kHeads * 4, l);
+      st_cluster_f32(st + 2 * kHeads * 4, lf);
+      __syncwarp();
+      if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_STF)));
+      ++stn;
+    }
+    (void)ok;
+  } else if (rank == 1 && warp >= 2) {
+    // ================= rank 1 epilogue: O rescale, tails, output ================
+    const float *afac = reinterpret_cast<const float *>(smem + kOffA);
+    const volatile float *stats = reinterpret_cast<const volatile float *>(smem + kOffStats);
+    volatile int *decision = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    int g = 0, stn = 0;
+    bool ok = true;
+    for (int si = seg_lo; si < seg_hi; ++si) {
+      const int4 sg = segs[si];
+      const int b = sg.x, tb = sg.y, te = sg.z, wslot = sg.w;
+      const int64_t orow = int64_t(b) * kHeads + row;
+      if (te <= tb) {  // empty request
+        uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv);
+        for (int c = 0; c < kDv / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+        p.lse[orow] = -INFINITY;
+        continue;
+      }
+      const int L = p.seqlens[b];
+      const int nb = num_blocks(tb, te);
+      for (int j = 0; j < nb; ++j, ++g) {
+        const int w0 = (tb / kBlk) * kBlk + j * kBlk;
+        const int pb = g & 1, s = g % kNst;
+        ok = ok && cx.wait(B_PF0 + pb, uint32_t((g >> 1) & 1));
+        const uint32_t flag = misc[4 + pb * 4 + q4];
+        if (flag && j > 0) {
+          // the maximum of some of this warp's rows moved: scale their O rows
+          // (after PV(g-1); PV(g) waits for this warp's arrival below)
+          ok = ok && cx.wait(B_PVD0 + ((g - 1) & 1), uint32_t(((g - 1) >> 1) & 1));
           tc_fence_after();
+          const float a = afac[pb * kHeads + row];
           float v[32];
-          for (int c = 0; c < 256; c += 32) {
-            tmem_ld32(tO + lane_off + c, v);
+#pragma unroll 1
+          for (int c = 0; c < kDv; c += 32) {
+            tmem_ld32(tmem + kTO + lane_off + c, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= a;
-            tmem_st32(tO + lane_off + c, v);
+            tmem_st32(tmem + kTO + lane_off + c, reinterpret_cast<const uint32_t *>(v));
           }
         }
-        // rows of the block past the end of the request hold arbitrary bytes:
-        // zero them in this rank's value chunks (the QK of this block is done)
         if (w0 + kBlk > L) {
-          const int t_lo = L - w0;  // >= 1 because w0 < te <= L
-          uint8_t *stage = smem + (sKV - cx.sbase) + uint32_t(g % nst) * stage_bytes;
-          const int pieces = 4 * (kBlk - t_lo) * 8;
+          // V rows of the block past the end of the request hold arbitrary
+          // bytes (0 * NaN would poison O): zero them in this rank's copy
+          ok = ok && cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u);
+          const int t_lo = max(0, min(kBlk, L - w0));
+          const int nrow = kBlk - t_lo;
+          uint8_t *stage = smem + kOffRing + uint32_t(s) * kMainBytes;
+          const int pieces = 8 * nrow * 8;
           for (int i = threadIdx.x - 64; i < pieces; i += 128) {
-            const int c = i / ((kBlk - t_lo) * 8), rest = i - c * ((kBlk - t_lo) * 8);
-            *reinterpret_cast<int4 *>(stage + c * (kBlk * 128) + (t_lo + (rest >> 3)) * 128 + (rest & 7) * 16) =
+            const int c = i / (nrow * 8), rest = i - c * (nrow * 8);
+            *reinterpret_cast<int4 *>(stage + c * kChunkBytes + (t_lo + (rest >> 3)) * 128 + (rest & 7) * 16) =
                 make_int4(0, 0, 0, 0);
           }
-          ptx::fence_proxy_async_smem();
-          asm volatile("bar.sync 1, 128;" ::: "memory");
         }
+        ptx::fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(cx.bar(B_OR0 + pb));
       }
-      // ---- segment end: wait for the last PV; this thread holds its row's stats ----
-      ok = ok && cx.wait(B_PVD0 + int((g - 1) & 1), uint32_t(((g - 1) >> 1) & 1));
+      // ---- segment end: row statistics from rank 0, last PV, then output ----
+      ok = ok && cx.wait(B_STF, uint32_t(stn & 1));
+      const float mref = stats[row], l = stats[kHeads + row], lf = stats[2 * kHeads + row];
+      __syncwarp();
+      if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_STE)));
+      ++stn;
+      ok = ok && cx.wait(B_PVD0 + ((g - 1) & 1), uint32_t(((g - 1) >> 1) & 1));
       tc_fence_after();
       if (wslot < 0) {
         const float inv = 1.f / l;
         float v[32];
-        for (int c = 0; c < 256; c += 32) {
-          tmem_ld32(tO + lane_off + c, v);
+#pragma unroll 1
+        for (int c = 0; c < kDv; c += 32) {
+          tmem_ld32(tmem + kTO + lane_off + c, v);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) pk[i / 2] = ptx::pack_bf16(v[i] * inv, v[i + 1] * inv);
-          uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256 + c);
+          uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + c);
 #pragma unroll
           for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
-        if (rank == 0) p.lse[orow] = (mref + log2f(lf)) * kLn2;
+        p.lse[orow] = (mref + log2f(lf)) * kLn2;
       } else {
-        float *ps = p.partials + int64_t(wslot) * p.slot_floats;
-        float v[32];
-        for (int c = 0; c < 256; c += 32) {
-          tmem_ld32(tO + lane_off + c, v);
-          float4 *d4 = reinterpret_cast<float4 *>(ps + row * kDv + rank * 256 + c);
+        // ---- split: publish the partial, the last split merges ----
+        const int nsp = plan[off.nsplit + b], s0 = plan[off.slot0 + b];
+        ptx::named_bar(1, 128);  // previous use of the decision word is over
+        if (threadIdx.x == 64)
+          *decision = (!*cx.abort && ld_acquire_gpu(p.item_cnt + b) == nsp - 1) ? 1 : 0;
+        ptx::named_bar(1, 128);
+        // all other splits already published: merge from TMEM without writing this one
+        const bool own_tmem = *decision != 0;
+        bool last = own_tmem;
+        if (!own_tmem) {
+          float *ps = p.partials + int64_t(wslot) * p.slot_floats;
+          float v[32];
+#pragma unroll 1
+          for (int c = 0; c < kDv; c += 32) {
+            tmem_ld32(tmem + kTO + lane_off + c, v);
+            float4 *d4 = reinterpret_cast<float4 *>(ps + row * kDv + c);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
-        if (rank == 0) {
+            for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
           ps[kHeads * kDv + row] = mref;
           ps[kHeads * kDv + kHeads + row] = l;
           ps[kHeads * kDv + 2 * kHeads + row] = lf;
-        }
-      }
-      tc_fence_before();
-      // the O accumulator may be overwritten by the next segment's first PV
-      __syncwarp();
-      if (wslot >= 0) {
-        // both ranks' partial writes, then one release-acquire arrival per pair
-        const int nsp = plan[off.nsplit + b], s0 = plan[off.slot0 + b];
-        ptx::named_bar(1, 128);
-        int last = 0;
-        if (rank == 1) {
-          if (threadIdx.x == 64) {
-            __threadfence();
-            arrive_remote(cx.peer_addr(cx.bar(B_PAIR)));
-          }
-          ok = ok && cx.wait(B_GO, uint32_t(pairn & 1));
-          last = *reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
-        } else {
+          ptx::named_bar(1, 128);
           if (threadIdx.x == 64) {
             int lst = 0;
-            if (cx.wait(B_PAIR, uint32_t(pairn & 1)) && !*cx.abort)
+            if (!*cx.abort) {
+              __threadfence();
               lst = ptx::atom_add_acq_rel_gpu(p.item_cnt + b, 1) == nsp - 1 ? 1 : 0;
-            *reinterpret_cast<volatile int *>(smem + kOffMisc + 8) = lst;
-            st_cluster_u32(cx.peer_addr(cx.sbase + kOffMisc + 8), uint32_t(lst));
-            arrive_remote(cx.peer_addr(cx.bar(B_GO)));
-            if (lst) p.item_cnt[b] = 0;
+            }
+            *decision = lst;
           }
           ptx::named_bar(1, 128);
-          last = *reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+          last = *decision != 0;
         }
-        ++pairn;
         if (last) {
-          // merge this rank's 256 columns of every split, in split order
-          __threadfence();
+          if (threadIdx.x == 64) p.item_cnt[b] = 0;  // ready for the next launch
+          // merge all splits of this row in slot order (same arithmetic whichever split merges)
           float Mx = -INFINITY;
-          for (int s = 0; s < nsp; ++s)
-            Mx = fmaxf(Mx, __ldcg(p.partials + int64_t(s0 + s) * p.slot_floats + kHeads * kDv + row));
+          for (int s = 0; s < nsp; ++s) {
+            const float ms = (own_tmem && s0 + s == wslot)
+                                 ? mref
+                                 : __ldcg(p.partials + int64_t(s0 + s) * p.slot_floats + kHeads * kDv + row);
+            Mx = fmaxf(Mx, ms);
+          }
           const float Mu = Mx == -INFINITY ? 0.f : Mx;
           float lam = 0.f, lamf = 0.f;
           for (int s = 0; s < nsp; ++s) {
-            const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats;
-            const float f = exp2f(__ldcg(ps + kHeads * kDv + row) - Mu);
-            lam += __ldcg(ps + kHeads * kDv + kHeads + row) * f;
-            lamf += __ldcg(ps + kHeads * kDv + 2 * kHeads + row) * f;
+            float ms, ls, lfs;
+            if (own_tmem && s0 + s == wslot) {
+              ms = mref;
+              ls = l;
+              lfs = lf;
+            } else {
+              const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats + kHeads * kDv;
+              ms = __ldcg(ps + row);
+              ls = __ldcg(ps + kHeads + row);
+              lfs = __ldcg(ps + 2 * kHeads + row);
+            }
+            const float f = exp2f(ms - Mu);
+            lam += ls * f;
+            lamf += lfs * f;
           }
           const float inv = 1.f / lam;
-          for (int c = 0; c < 256; c += 8) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int c = 0; c < kDv; c += 32) {
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
             for (int s = 0; s < nsp; ++s) {
-              const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats;
-              const float f = exp2f(__ldcg(ps + kHeads * kDv + row) - Mu);
-              const float4 *src = reinterpret_cast<const float4 *>(ps + row * kDv + rank * 256 + c);
-              const float4 x = __ldcg(src), y = __ldcg(src + 1);
-              acc[0] += x.x * f;
-              acc[1] += x.y * f;
-              acc[2] += x.z * f;
-              acc[3] += x.w * f;
-              acc[4] += y.x * f;
-              acc[5] += y.y * f;
-              acc[6] += y.z * f;
-              acc[7] += y.w * f;
+              float v[32];
+              float ms;
+              if (own_tmem && s0 + s == wslot) {
+                tmem_ld32(tmem + kTO + lane_off + c, v);
+                ms = mref;
+              } else {
+                const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats;
+                const float4 *src = reinterpret_cast<const float4 *>(ps + row * kDv + c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 x = __ldcg(src + i);
+                  v[4 * i] = x.x;
+                  v[4 * i + 1] = x.y;
+                  v[4 * i + 2] = x.z;
+                  v[4 * i + 3] = x.w;
+                }
+                ms = __ldcg(ps + kHeads * kDv + row);
+              }
+              const float f = exp2f(ms - Mu);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] += v[i] * f;
             }
-            *reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256 + c) =
-                make_uint4(ptx::pack_bf16(acc[0] * inv, acc[1] * inv), ptx::pack_bf16(acc[2] * inv, acc[3] * inv),
-                           ptx::pack_bf16(acc[4] * inv, acc[5] * inv), ptx::pack_bf16(acc[6] * inv, acc[7] * inv));
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) pk[i / 2] = ptx::pack_bf16(acc[i] * inv, acc[i + 1] * inv);
+            uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
-          if (rank == 0) p.lse[orow] = (Mx + log2f(lamf)) * kLn2;
+          p.lse[orow] = (Mx + log2f(lamf)) * kLn2;
         }
       }
+      tc_fence_before();  // O reads done before the next segment's first PV overwrites it
     }
     (void)ok;
   }
@@ -669,13 +725,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();
+  if (threadIdx.x == 0 && *cx.abort) {
+    // after a give-up, wait (bounded) for the copies still in flight into this CTA
+    const int n = int(misc[3]);
+    for (int i = max(0, n - kNst); i < n; ++i)
+      ptx::mbar_wait(cx.bar(B_KVF + i % kNst), uint32_t(i / kNst) & 1u, nullptr, kWaitCycles);
+  }
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u));
-  }
-  if (tr && lane == 0) {
-    const int slot = warp == 0 ? 12 : (warp == 1 ? 11 : 10);
-    atomicAdd(reinterpret_cast<unsigned long long *>(tr + slot), (unsigned long long)(clock64() - tk0));
   }
   if (tr && threadIdx.x == 0) {
     tr[14] = seg_hi - seg_lo;
@@ -689,23 +748,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 int launch_mla(const DecodeArgs &a) {
   const skd_shape_t &s = a.shape;
   if (s.page_size % kBlk != 0) return SKD_EUNSUPPORTED;  // 64-token blocks must not straddle pages
-  CUtensorMap tq[2], tkv[2];
-  // dims (innermost first): 64 columns, rows (tokens or heads), 9 column chunks
-  const cuuint64_t gq[3] = {64, cuuint64_t(s.batch) * kHeads, 9};
-  const cuuint64_t sq[2] = {cuuint64_t(kDk) * 2, 128};
+  // latent cache viewed as {64 columns, rows (page*P + slot), 9 column chunks}
+  CUtensorMap tmain, trope;
   const cuuint64_t gk[3] = {64, cuuint64_t(s.num_pages) * s.page_size, 9};
   const cuuint64_t sk[2] = {cuuint64_t(s.v_row_stride) * 2, 128};
   const cuuint32_t es[3] = {1, 1, 1};
-  for (int r = 0; r < 2; ++r) {
-    const cuuint32_t nch = r == 0 ? 4 : 5;
-    const cuuint32_t bq[3] = {64, kHeads, nch}, bk[3] = {64, kBlk, nch};
-    if (encode_tiled(&tq[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.q), gq, sq, bq, es,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-        encode_tiled(&tkv[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k), gk, sk, bk, es,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return SKD_EINVAL;
-  }
+  const cuuint32_t bmain[3] = {64, kBlk, 8}, brope[3] = {64, kBlk, 1};
+  if (encode_tiled(&tmain, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k), gk, sk, bmain, es,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode_tiled(&trope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k), gk, sk, brope, es,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return SKD_EINVAL;
   Params p;
+  p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.page_table = a.page_table;
   p.seqlens = a.seqlens;
   p.plan = a.plan;
@@ -723,22 +778,14 @@ int launch_mla(const DecodeArgs &a) {
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.slot_floats = a.wl.slot_floats;
   p.trace = static_cast<long long *>(trace_buffer(2 * a.n_ctas));
-  // stages per rank: shared memory = fixed region + Q + stages (both ranks get the same size)
-  const int budget = 227 * 1024 - 1024;
-  p.nst0 = std::min(kMaxSt, (budget - kOffQ - 4 * kHeads * 128) / (4 * kBlk * 128));
-  p.nst1 = std::min(kMaxSt, (budget - kOffQ - 5 * kHeads * 128) / (5 * kBlk * 128));
-  if (p.nst0 < 2 || p.nst1 < 2) return SKD_EUNSUPPORTED;
-  const int smem0 = kOffQ + 4 * kHeads * 128 + p.nst0 * 4 * kBlk * 128;
-  const int smem1 = kOffQ + 5 * kHeads * 128 + p.nst1 * 5 * kBlk * 128;
-  const int smem = std::max(smem0, smem1) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
         cudaSuccess)
       return SKD_ECUDA;
     attr_set = true;
   }
-  mla_decode_kernel<<<2 * a.n_ctas, kThreads, smem, a.stream>>>(tq[0], tq[1], tkv[0], tkv[1], p);
+  mla_decode_kernel<<<2 * a.n_ctas, kThreads, kSmemBytes, a.stream>>>(tmain, trope, p);
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 
