@@ -46,6 +46,8 @@ def _args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_gqa")
     ap.add_argument("--mode", choices=["streamk", "round_robin"], default="streamk")
+    ap.add_argument("--seg-cost", type=int, default=None,
+                    help="planner's per-segment cost in granules (default: the library's per-kind default)")
     ap.add_argument("--n-ctas", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample (cpu_baseline)")
@@ -250,7 +252,8 @@ def run_ours(a):
     sl = torch.from_numpy(w.seqlens).to(dev)
     shape = skd.make_shape(q, k, v, pt, scale=w.scale, causal=w.causal)
     n = a.n_ctas or skd.default_ctas(shape)
-    plan_h = skd.plan(w.seqlens, shape.num_kv_heads, w.page_size, n, a.mode)
+    seg_cost = 0 if a.mode != "streamk" else (skd.default_seg_cost(shape) if a.seg_cost is None else a.seg_cost)
+    plan_h = skd.plan(w.seqlens, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)
     plan_d = plan_h.to(dev)
     ws = skd.workspace(shape, n, dev)
     out = torch.empty(w.batch, w.q_tokens, w.num_q_heads, w.head_dim_v, dtype=torch.bfloat16, device=dev)
@@ -317,7 +320,7 @@ def run_ours(a):
         plan_dd = torch.empty_like(plan_d)
 
         def e2e_step():
-            p = skd.plan(sl_h, shape.num_kv_heads, w.page_size, n, a.mode)  # host planner
+            p = skd.plan(sl_h, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)  # host planner
             plan_pin.copy_(p)
             q_d.copy_(q_h, non_blocking=True)
             pt_d.copy_(pt_h, non_blocking=True)
@@ -361,7 +364,7 @@ def run_ours(a):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
         "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
-                   "n_ctas": n, "plan": a.mode, "algorithmic_bytes": alg_bytes,
+                   "n_ctas": n, "plan": a.mode, "seg_cost": seg_cost, "algorithmic_bytes": alg_bytes,
                    "l2": "no flush: KV per step is larger than L2 (129 MB)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

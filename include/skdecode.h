@@ -142,6 +142,22 @@ int skd_decode_plan_device(const int32_t *seqlens_dev, int batch, int num_kv_hea
                            int page_size, int n_ctas, void *plan_dev, size_t plan_bytes,
                            void *stream);
 
+/* Weighted Stream-K split (an extension: the pages charge nothing per
+ * segment). Every non-empty work item is preceded by `seg_cost` virtual
+ * granules that carry no tokens, standing for the fixed time a CTA spends per
+ * segment (loading the item's queries, writing its output or partial state);
+ * the equal split of triton.csdn.net's closing summary then runs over the
+ * virtual total, so a CTA whose range crosses many item boundaries gets fewer
+ * tokens. seg_cost = 0 gives exactly skd_decode_plan's STREAMK plan. Host and
+ * device variants produce identical bytes. 0 <= seg_cost <= 65536, else
+ * SKD_EINVAL; other arguments and errors as skd_decode_plan /
+ * skd_decode_plan_device. The value used is stored in the plan header. */
+int skd_decode_plan_weighted(const int32_t *seqlens_host, int batch, int num_kv_heads, int page_size,
+                             int n_ctas, int seg_cost, void *plan_host, size_t plan_bytes);
+int skd_decode_plan_weighted_device(const int32_t *seqlens_dev, int batch, int num_kv_heads, int page_size,
+                                    int n_ctas, int seg_cost, void *plan_dev, size_t plan_bytes,
+                                    void *stream);
+
 /* ---- workspace --------------------------------------------------------- */
 
 /* Bytes of the workspace skd_decode_attention needs for this shape and grid:

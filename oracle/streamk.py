@@ -14,6 +14,11 @@ streamk_split
     segments. "MeldKernel：动态负载下跨 SM 融合内核（SOSP 2026）", core method:
     the split is decided at run time from the real sequence lengths.
 
+    Optional ``seg_cost`` (an extension; the pages charge nothing per
+    segment): each non-empty item is preceded by ``seg_cost`` virtual granules
+    that hold no tokens, so the equal split runs over tokens plus a fixed cost
+    per item start. ``seg_cost = 0`` is the split above.
+
 round_robin_split
     Whole work items dealt to workers in turn, the way the GLM-5.2 decode
     article ("GLM-5.2-FP8 ... B300", MegaRTP KernelPlan paragraph) deals tile
@@ -35,7 +40,7 @@ def _ceil_div(a: int, b: int) -> int:
 
 
 def streamk_split(seqlens: Sequence[int], num_kv_heads: int, n_ctas: int,
-                  granule: int = 16) -> Dict:
+                  granule: int = 16, seg_cost: int = 0) -> Dict:
     """Stream-K one-wave split.
 
     Returns a dict with
@@ -47,13 +52,15 @@ def streamk_split(seqlens: Sequence[int], num_kv_heads: int, n_ctas: int,
     length 0 occupies no work; it is a segment of the first CTA whose chunk ends
     after its position (the last CTA if none).
     """
-    if n_ctas <= 0 or num_kv_heads <= 0 or granule <= 0:
-        raise ValueError("n_ctas, num_kv_heads and granule must be positive")
+    if n_ctas <= 0 or num_kv_heads <= 0 or granule <= 0 or seg_cost < 0:
+        raise ValueError("n_ctas, num_kv_heads and granule must be positive, seg_cost >= 0")
     L = [int(x) for x in seqlens]
     items = [(b * num_kv_heads + h, L[b]) for b in range(len(L)) for h in range(num_kv_heads)]
     starts = []
     pos = 0
     for _, length in items:
+        if length > 0:
+            pos += seg_cost  # the item's virtual start cost, before its tokens
         starts.append(pos)
         pos += _ceil_div(length, granule)
     total = pos

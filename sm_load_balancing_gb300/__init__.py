@@ -23,7 +23,7 @@ from ._native import (SKD_DEVERR_PAGE, SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN,
                       SKD_DEVERR_TIMEOUT, SKD_GRANULE, SkdError)
 
 __all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention", "read_error",
-           "sm_count", "default_ctas", "make_shape", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
+           "sm_count", "default_ctas", "default_seg_cost", "make_shape", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
            "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT"]
 
 _MODES = {"streamk": N.SKD_PLAN_STREAMK, "round_robin": N.SKD_PLAN_ROUND_ROBIN}
@@ -48,14 +48,28 @@ def default_ctas(shape: Optional[N.Shape] = None, device: Optional[int] = None) 
     return n // 2 if (shape is not None and shape.kind == N.SKD_KIND_MLA) else n
 
 
+# Fixed per-segment cost of the absorbed-MLA kernel in granules of KV work:
+# loading a request's 128 query rows into TMEM and draining its 128x512
+# accumulator take about as long as this many granules of streaming.
+MLA_SEG_COST = 40
+
+
+def default_seg_cost(shape: Optional[N.Shape] = None) -> int:
+    """Per-segment cost (granules) the planner charges by default: the MLA
+    kernel pays a large fixed cost per segment, the GQA kernel a negligible one."""
+    return MLA_SEG_COST if (shape is not None and shape.kind == N.SKD_KIND_MLA) else 0
+
+
 def plan_bytes(batch: int, num_kv_heads: int, n_ctas: int) -> int:
     return int(N.lib().skd_plan_bytes(batch, num_kv_heads, n_ctas))
 
 
 def plan(seqlens, num_kv_heads: int, page_size: int, n_ctas: Optional[int] = None,
-         mode: str = "streamk") -> torch.Tensor:
+         mode: str = "streamk", seg_cost: int = 0) -> torch.Tensor:
     """Host planner. ``seqlens``: CPU int32 tensor (or anything torch.as_tensor
-    takes). Returns the plan as a CPU int32 tensor; copy it to the device."""
+    takes). ``seg_cost``: virtual granules charged per work item (Stream-K
+    only; 0 = the plain equal split). Returns the plan as a CPU int32 tensor;
+    copy it to the device."""
     sl = torch.as_tensor(seqlens, dtype=torch.int32).contiguous()
     if sl.device.type != "cpu":
         raise ValueError("plan() takes host seqlens; use plan_device() for device seqlens")
@@ -64,24 +78,32 @@ def plan(seqlens, num_kv_heads: int, page_size: int, n_ctas: Optional[int] = Non
     if nb == 0:
         raise ValueError("invalid batch / num_kv_heads / n_ctas")
     out = torch.zeros(nb // 4, dtype=torch.int32)
-    N.check("skd_decode_plan", N.lib().skd_decode_plan(
-        sl.data_ptr(), int(sl.numel()), int(num_kv_heads), int(page_size), n, _MODES[mode],
-        out.data_ptr(), nb))
+    if mode == "streamk":
+        N.check("skd_decode_plan_weighted", N.lib().skd_decode_plan_weighted(
+            sl.data_ptr(), int(sl.numel()), int(num_kv_heads), int(page_size), n, int(seg_cost),
+            out.data_ptr(), nb))
+    else:
+        if seg_cost:
+            raise ValueError("seg_cost applies to the streamk mode only")
+        N.check("skd_decode_plan", N.lib().skd_decode_plan(
+            sl.data_ptr(), int(sl.numel()), int(num_kv_heads), int(page_size), n, _MODES[mode],
+            out.data_ptr(), nb))
     return out
 
 
 def plan_device(seqlens: torch.Tensor, num_kv_heads: int, page_size: int, n_ctas: int,
                 out: Optional[torch.Tensor] = None,
-                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Device planner (graph capturable). ``seqlens``: CUDA int32 tensor."""
+                stream: Optional[torch.cuda.Stream] = None, seg_cost: int = 0) -> torch.Tensor:
+    """Device planner (graph capturable), byte-identical to ``plan``.
+    ``seqlens``: CUDA int32 tensor."""
     if seqlens.device.type != "cuda" or seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
         raise ValueError("seqlens must be a contiguous CUDA int32 tensor")
     nb = plan_bytes(int(seqlens.numel()), num_kv_heads, n_ctas)
     if out is None:
         out = torch.empty(nb // 4, dtype=torch.int32, device=seqlens.device)
-    N.check("skd_decode_plan_device", N.lib().skd_decode_plan_device(
+    N.check("skd_decode_plan_weighted_device", N.lib().skd_decode_plan_weighted_device(
         seqlens.data_ptr(), int(seqlens.numel()), int(num_kv_heads), int(page_size), int(n_ctas),
-        out.data_ptr(), out.numel() * 4, _stream_ptr(stream)))
+        int(seg_cost), out.data_ptr(), out.numel() * 4, _stream_ptr(stream)))
     return out
 
 

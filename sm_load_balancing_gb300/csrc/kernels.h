@@ -34,7 +34,7 @@ struct DecodeArgs {
 
 int launch_gqa(const DecodeArgs &a);
 int launch_mla(const DecodeArgs &a);
-int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n_ctas, int32_t *plan,
+int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n_ctas, int seg_cost, int32_t *plan,
                        cudaStream_t stream);
 
 // cuTensorMapEncodeTiled, looked up through the runtime (no libcuda link).

@@ -38,7 +38,12 @@ namespace skd {
 namespace {
 
 constexpr int kHeads = 128, kDk = 576, kDv = 512, kBlk = 64;
-constexpr int kThreads = 192;  // warp 0 TMA (rank 0), warp 1 MMA, warps 2-5 epilogue
+// warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quarter),
+// warps 10-11 (rank 0) two more MMA issuers: one thread issues a tcgen05.mma
+// about every 90-120 cycles whatever its size, so the 36 small score MMAs of a
+// block are spread over three issuing warps
+constexpr int kThreads = 384;
+constexpr int kQkIssuers = 3;
 constexpr int kNst = 3;        // KV ring stages
 constexpr float kTau = 8.f;    // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994531f;
@@ -48,33 +53,40 @@ constexpr int kTraceWords = SKD_TRACE_RECORD_BYTES / 8;
 // stores address the partner's buffers by the local offset)
 constexpr uint32_t kChunkBytes = kBlk * 128;       // 64 columns x 64 tokens, bf16, SW128
 constexpr uint32_t kMainBytes = 8 * kChunkBytes;   // value columns [0, 512) of one block
+constexpr uint32_t kPBytes = kHeads * kBlk * 2;    // P of one block: 128 rows x 128 B
+constexpr uint32_t kQuarterP = kPBytes / 4;        // the 32 rows of one epilogue warp
 constexpr uint32_t kOffRing = 0;                   // [kNst][64 KB], both ranks
-constexpr uint32_t kOffRope = kNst * kMainBytes;   // rank 0: [kNst][8 KB] columns [512, 576)
+constexpr uint32_t kOffRope = kNst * kMainBytes;   // rank 0: [2][8 KB] columns [512, 576)
+constexpr uint32_t kOffStage = kOffRope + 2 * kChunkBytes;  // rank 0: P staging [4 warps][4 KB]
 constexpr uint32_t kOffP = kNst * kMainBytes;      // rank 1: P [2][128 rows][64 tok] bf16, SW128
-constexpr uint32_t kPBytes = kHeads * kBlk * 2;
 constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;  // mbarriers
 constexpr int kNumBar = 24;
-constexpr uint32_t kOffA = kOffBar + kNumBar * 8;  // rank 1: rescale factors [2][128] fp32
-constexpr uint32_t kOffStats = kOffA + 2 * kHeads * 4;  // rank 1: m, l, lf [3][128] fp32
+// per (P buffer, warp): 32 rescale factors + a flag word, padded to 144 bytes
+// (rank 0 stages its copy in the slots of P buffer 0)
+constexpr uint32_t kFaBytes = 144;
+constexpr uint32_t kOffFa = kOffBar + kNumBar * 8;
+constexpr uint32_t kOffStats = kOffFa + 8 * kFaBytes;  // rank 1: m, l, lf [3][128] fp32
 constexpr uint32_t kOffMisc = kOffStats + 3 * kHeads * 4;
-// misc words: 0 tmem base, 1 abort, 2 merge decision, 3 blocks issued by the
-// producer, 4..11 rescale flags [P buffer][quarter]
+// misc words: 0 tmem base, 1 abort, 2 merge decision, 3 blocks issued by the producer
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kOffRope + kNst * kChunkBytes <= kOffBar, "rope ring overlaps the barriers");
+static_assert(kOffStage + 4 * kQuarterP <= kOffBar, "P staging overlaps the barriers");
+static_assert(kOffFa % 16 == 0 && kFaBytes % 16 == 0, "bulk copies need 16-byte alignment");
 
 // TMEM columns
 constexpr uint32_t kTQ = 0;                     // rank 0: Q, 288 columns (2 bf16 per column)
-constexpr uint32_t kTS0 = 384, kTS1 = 448;      // rank 0: score tiles, 64 columns each
+constexpr uint32_t kTS = 320;                   // rank 0: 3 partial score tiles (one per issuer), 64 columns each
 constexpr uint32_t kTO = 0;                     // rank 1: O, 512 columns
 
 enum {
   B_KVF = 0,            // [kNst] block landed (rank 0: 72 KB, rank 1: 64 KB)
-  B_KVE = kNst,         // [kNst] rank 0: stage free (rank 0 QK done + rank 1 PV done)
-  B_QF = 2 * kNst,      // rank 0: Q of the segment is in TMEM (4 epilogue warps)
-  B_SF0, B_SF1,         // rank 0: score tile complete
-  B_SE0, B_SE1,         // rank 0: score tile read out (4)
-  B_PF0, B_PF1,         // rank 1: P, factors and flags of the block landed (4 remote)
+  B_KVE = kNst,         // [kNst] stage free (rank 0: QK done, rank 1: PV done)
+  B_RE0 = 2 * kNst,     // [2] rank 0: rope slot free (QK done)
+  B_QF = B_RE0 + 2,     // rank 0: Q of the segment is in TMEM (4 epilogue warps)
+  B_Q0,                 // both: the first segment's Q is in TMEM (4 arrivals from rank 0, once)
+  B_SF0, B_SF1,         // rank 0: score tiles complete (3 issuers; B_SF1 unused)
+  B_SE0, B_SE1,         // rank 0: score tiles read out (8 epilogue warps; B_SE1 unused)
+  B_PF0, B_PF1,         // rank 1: P, factors and flags of the block landed (4 bulk copies)
   B_PVD0, B_PVD1,       // both: PV of the block that used P buffer 0/1 complete
   B_OR0, B_OR1,         // rank 1: O rescaled / V tail zeroed, PV may run (4)
   B_STF,                // rank 1: segment statistics landed (4 remote)
@@ -113,21 +125,54 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-__device__ __forceinline__ void arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+// the same without release semantics (the data follows through the async proxy)
+__device__ __forceinline__ void arrive_expect_tx_remote_relaxed(uint32_t cluster_addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
                "r"(bytes)
                : "memory");
+}
+// copy `bytes` of this CTA's shared memory to the partner's (cluster address),
+// counted on the partner's barrier `bar_cluster`
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// fp32 store that asks L2 to keep the line (partials are read again at the kernel's end)
+__device__ __forceinline__ void st_keep(float *p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// 2-D tiled store shared -> global (bulk group)
+__device__ __forceinline__ void tma_store2(const CUtensorMap *m, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -148,7 +193,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -224,40 +268,49 @@ __device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap *m, uint32_
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
       : "memory");
 }
-// same box into every CTA of `mask` (same offset; each CTA's barrier at `bar`'s offset counts its bytes)
-__device__ __forceinline__ void tma3_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2,
-                                        uint16_t mask, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::"
-      "cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask), "l"(pol)
-      : "memory");
+
+// trace words 2..11: cycles spent waiting, per barrier kind (lane 0 of each waiting warp)
+__device__ __forceinline__ int trace_word(int i) {
+  return i < B_KVE ? 2 : i < B_QF ? 3 : i == B_QF ? 4 : i <= B_SF1 ? 5 : i <= B_SE1 ? 6 : i <= B_PF1 ? 7
+       : i <= B_PVD1 ? 8 : i <= B_OR1 ? 9 : i == B_STF ? 10 : 11;
 }
 
 struct Ctx {
   uint32_t sbase, peer;  // own shared base; peer rank
   volatile int *abort;
   int32_t *err;
+  long long *tr;  // per-CTA trace record or null
   __device__ uint32_t bar(int i) const { return sbase + kOffBar + 8u * i; }
   __device__ uint32_t peer_addr(uint32_t local) const { return mapa(local, peer); }
   // bounded wait with cluster-scope acquire; on timeout flag both ranks
   __device__ bool wait(int i, uint32_t parity) const {
     const uint32_t b = bar(i);
-    if (try_wait_cluster(b, parity)) return true;
     const long long t0 = clock64();
+    if (try_wait_cluster(b, parity)) {
+      if (tr && (threadIdx.x & 31) == 0)
+        atomicAdd(reinterpret_cast<unsigned long long *>(tr + trace_word(i)), (unsigned long long)(clock64() - t0));
+      return true;
+    }
     uint32_t n = 0;
+    bool ok = true;
     while (!try_wait_cluster(b, parity)) {
       if ((++n & 255u) == 0) {
-        if (*abort) return false;
+        if (*abort) {
+          ok = false;
+          break;
+        }
         if (clock64() - t0 > kWaitCycles) {
           *abort = 1;
           st_cluster_u32(peer_addr(sbase + kOffMisc + 4), 1u);
           atomicOr(err, SKD_DEVERR_TIMEOUT);
-          return false;
+          ok = false;
+          break;
         }
       }
     }
-    return true;
+    if (tr && (threadIdx.x & 31) == 0)
+      atomicAdd(reinterpret_cast<unsigned long long *>(tr + trace_word(i)), (unsigned long long)(clock64() - t0));
+    return ok;
   }
 };
 
@@ -266,6 +319,7 @@ __device__ __forceinline__ int num_blocks(int tb, int te) { return (te + kBlk - 
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmain, const __grid_constant__ CUtensorMap trope,
+                      const __grid_constant__ CUtensorMap tpart, const __grid_constant__ CUtensorMap tout,
                       const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -299,22 +353,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNst; ++s) {
       ptx::mbar_init(cx.bar(B_KVF + s), 1);
-      ptx::mbar_init(cx.bar(B_KVE + s), 2);
+      ptx::mbar_init(cx.bar(B_KVE + s), rank == 0 ? kQkIssuers : 1);
     }
-    ptx::mbar_init(cx.bar(B_QF), 4);
-    ptx::mbar_init(cx.bar(B_SF0), 1);
+    ptx::mbar_init(cx.bar(B_RE0), 1);
+    ptx::mbar_init(cx.bar(B_RE0 + 1), 1);
+    ptx::mbar_init(cx.bar(B_QF), 8);
+    ptx::mbar_init(cx.bar(B_Q0), 4);
+    ptx::mbar_init(cx.bar(B_SF0), kQkIssuers);
     ptx::mbar_init(cx.bar(B_SF1), 1);
-    ptx::mbar_init(cx.bar(B_SE0), 4);
-    ptx::mbar_init(cx.bar(B_SE1), 4);
+    ptx::mbar_init(cx.bar(B_SE0), 8);
+    ptx::mbar_init(cx.bar(B_SE1), 8);
     ptx::mbar_init(cx.bar(B_PF0), 4);
     ptx::mbar_init(cx.bar(B_PF1), 4);
     ptx::mbar_init(cx.bar(B_PVD0), 1);
     ptx::mbar_init(cx.bar(B_PVD1), 1);
-    ptx::mbar_init(cx.bar(B_OR0), 4);
-    ptx::mbar_init(cx.bar(B_OR1), 4);
+    ptx::mbar_init(cx.bar(B_OR0), 8);
+    ptx::mbar_init(cx.bar(B_OR1), 8);
     ptx::mbar_init(cx.bar(B_STF), 4);
-    ptx::mbar_init(cx.bar(B_STE), 4);
-    ptx::mbar_init(cx.bar(B_FIN), 1);
+    ptx::mbar_init(cx.bar(B_STE), 8);
+    ptx::mbar_init(cx.bar(B_FIN), rank == 0 ? kQkIssuers : 1);
     misc[1] = 0;
     misc[3] = 0;
     ptx::fence_mbar_init();
@@ -330,15 +387,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = misc[0];
 
   long long *const tr = p.trace ? p.trace + int64_t(blockIdx.x) * kTraceWords : nullptr;
+  cx.tr = tr;
   if (tr && threadIdx.x == 0) tr[0] = (long long)ptx::globaltimer_ns();
 
   const int q4 = warp & 3;                       // TMEM lane quarter of an epilogue warp
+  const int hc = (warp - 2) >> 2;                // its half (score columns on rank 0, O columns on rank 1)
   const int row = q4 * 32 + lane;                // query head of an epilogue thread
   const uint32_t lane_off = uint32_t(q4 * 32) << 16;
 
-  if (rank == 0 && warp == 0) {
-    // ============================ TMA producer ===============================
-    const uint64_t pol = ptx::policy_evict_first();
+  if (warp == 0) {
+    // ============================ TMA producers ==============================
+    // Each rank loads its own copy of the value columns into its own ring, so
+    // a rank-0 stage is free again as soon as its score MMAs are done; rank 1
+    // reads the block a few microseconds later, from L2, as its last reader.
+    const uint64_t pol = rank == 0 ? policy_evict_normal() : ptx::policy_evict_first();
     int g = 0;
     bool ok = true;
     for (int si = seg_lo; si < seg_hi && ok; ++si) {
@@ -360,27 +422,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             atomicOr(p.err, SKD_DEVERR_PAGE);
             pg = 0;
           }
-          ok = cx.wait(B_KVE + s, ph ^ 1u);
+          // after the first block, wait for the first Q to be loaded: its
+          // loads would otherwise queue behind the whole KV ring of every worker
+          ok = (g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
+               (rank == 1 || cx.wait(B_RE0 + (g & 1), uint32_t((g >> 1) & 1) ^ 1u));
           if (ok) {
             const int rowk = pg * p.P + (w0 % p.P);
-            ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), kMainBytes + kChunkBytes);
-            arrive_expect_tx_remote(cx.peer_addr(cx.bar(B_KVF + s)), kMainBytes);
-            tma3_mc(cx.sbase + kOffRing + s * kMainBytes, &tmain, cx.bar(B_KVF + s), 0, rowk, 0, 0x3, pol);
-            tma3(cx.sbase + kOffRope + s * kChunkBytes, &trope, cx.bar(B_KVF + s), 0, rowk, 8, pol);
+            ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), rank == 0 ? kMainBytes + kChunkBytes : kMainBytes);
+            tma3(cx.sbase + kOffRing + s * kMainBytes, &tmain, cx.bar(B_KVF + s), 0, rowk, 0, pol);
+            if (rank == 0)
+              tma3(cx.sbase + kOffRope + (g & 1) * kChunkBytes, &trope, cx.bar(B_KVF + s), 0, rowk, 8, pol);
             misc[3] = uint32_t(g + 1);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
     }
-    if (lane == 0) st_cluster_u32(cx.peer_addr(cx.sbase + kOffMisc + 12), misc[3]);
-  } else if (warp == 1) {
-    // ============================ MMA issuer =================================
+  } else if (warp == 1 || (rank == 0 && warp >= 10)) {
+    // ============================ MMA issuers ================================
     if (lane == 0) {
       int g = 0, qn = 0;
       bool ok = true;
       if (rank == 0) {
+        // issuer qi accumulates latent chunks [3 qi, 3 qi + 3) into its own
+        // partial score tile; the epilogue adds the three tiles
+        const int qi = warp == 1 ? 0 : warp - 9;
         constexpr uint32_t id_qk = idesc(kHeads, kBlk, 0);
+        const uint32_t dS = tmem + kTS + 64 * qi;
         for (int si = seg_lo; si < seg_hi && ok; ++si) {
           const int4 sg = segs[si];
           if (sg.z <= sg.y) continue;
@@ -389,24 +457,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ++qn;
           tc_fence_after();
           for (int j = 0; j < nb && ok; ++j, ++g) {
-            const int s = g % kNst, sb = g & 1;
-            if (!cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u) || !cx.wait(B_SE0 + sb, uint32_t((g >> 1) & 1) ^ 1u)) {
+            const int s = g % kNst;
+            if (!cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u) || !cx.wait(B_SE0, uint32_t(g & 1) ^ 1u)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
-            const uint32_t rope = cx.sbase + kOffRope + s * kChunkBytes;
-            const uint32_t dS = tmem + (sb ? kTS1 : kTS0);
+            const uint32_t rope = cx.sbase + kOffRope + (g & 1) * kChunkBytes;
 #pragma unroll
-            for (int c = 0; c < 9; ++c) {
+            for (int cc = 0; cc < 3; ++cc) {
+              const int c = 3 * qi + cc;
               const uint32_t bc = c < 8 ? ring + c * kChunkBytes : rope;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_ts(dS, tmem + kTQ + c * 32 + kk * 8, sdesc(bc + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
+                umma_ts(dS, tmem + kTQ + c * 32 + kk * 8, sdesc(bc + kk * 32, 16, 1024), id_qk, (cc | kk) != 0);
             }
-            umma_commit(cx.bar(B_SF0 + sb));
+            umma_commit(cx.bar(B_SF0));
             umma_commit(cx.bar(B_KVE + s));
+            if (qi == 2) umma_commit(cx.bar(B_RE0 + (g & 1)));
           }
         }
       } else {
@@ -432,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 umma_ss(tmem + kTO + h * 256, a, sdesc(ring + h * 4 * kChunkBytes + kk * (16 * 128), 8192, 1024),
                         id_pv, (j > 0 || kk > 0) ? 1u : 0u);
             }
-            umma_commit_mc(cx.bar(B_KVE + s), 0x1);   // rank 0 owns the ring
+            umma_commit(cx.bar(B_KVE + s));
             umma_commit_mc(cx.bar(B_PVD0 + pb), 0x3);  // P buffer free (rank 0), O ready (rank 1)
           }
         }
@@ -441,8 +510,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       umma_commit(cx.bar(B_FIN));
       ptx::mbar_wait(cx.bar(B_FIN), 0, nullptr, kWaitCycles);
     }
-  } else if (rank == 0 && warp >= 2) {
+  } else if (rank == 0 && warp >= 2 && warp < 10) {
     // ====================== rank 0 epilogue: online softmax ====================
+    // Warps w and w+4 share the 32 head rows of one TMEM lane quarter; warp
+    // half hc handles score columns [32 hc, 32 hc + 32) of every block. The
+    // two halves exchange their row maxima through shared memory, so both
+    // derive the same reference maximum, and keep separate partial sums.
+    float *xm = reinterpret_cast<float *>(smem + kOffStats);  // [2 halves][128 rows]
+    const int pair_bar = 2 + q4;
     int g = 0, stn = 0;
     bool ok = true;
     for (int si = seg_lo; si < seg_hi; ++si) {
@@ -450,96 +525,162 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int b = sg.x, tb = sg.y, te = sg.z;
       if (te <= tb) continue;
       const int nb = num_blocks(tb, te);
-      // Q row of this head into TMEM (the previous segment's score MMAs have
+      // Q of this head into TMEM, chunks [0, 5) by half 0 and [5, 9) by half
+      // 1, in one round of loads (the previous segment's score MMAs have
       // completed: this thread saw the score tile of its last block)
       {
         const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q) + (int64_t(b) * kHeads + row) * (kDk / 8);
-#pragma unroll 1
-        for (int c = 0; c < 9; c += 3) {
-          uint4 v[24];
+        const int c0 = hc == 0 ? 0 : 5, nc = hc == 0 ? 5 : 4;
+        uint4 v[40];
 #pragma unroll
-          for (int i = 0; i < 24; ++i) v[i] = __ldg(qrow + c * 8 + i);
+        for (int i = 0; i < 40; ++i)
+          if (i < nc * 8) v[i] = __ldg(qrow + c0 * 8 + i);
 #pragma unroll
-          for (int cc = 0; cc < 3; ++cc)
-            tmem_st32(tmem + kTQ + lane_off + (c + cc) * 32, reinterpret_cast<const uint32_t *>(v + cc * 8));
-        }
+        for (int c = 0; c < 5; ++c)
+          if (c < nc) tmem_st32(tmem + kTQ + lane_off + (c0 + c) * 32, reinterpret_cast<const uint32_t *>(v + c * 8));
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(cx.bar(B_QF));
+        if (lane == 0) {
+          ptx::mbar_arrive(cx.bar(B_QF));
+          if (g == 0 && hc == 0) {
+            ptx::mbar_arrive(cx.bar(B_Q0));
+            arrive_remote(cx.peer_addr(cx.bar(B_Q0)));
+          }
+        }
       }
-      float mref = -INFINITY, l = 0.f, lf = 0.f;
+      // the next segment's Q rows of this quarter go to L2 a few blocks before they are needed
+      int q_next = -1;
+      for (int sn = si + 1; sn < seg_hi; ++sn)
+        if (segs[sn].z > segs[sn].y) {
+          q_next = segs[sn].x;
+          break;
+        }
+      const int j_pref = max(0, nb - 8);
+      float mref = -INFINITY, l = 0.f, lf = 0.f;  // l, lf: this half's sums
+      const uint32_t stage = cx.sbase + kOffStage + uint32_t(q4) * kQuarterP;  // the quarter's P rows
+      const uint32_t fstage = cx.sbase + kOffFa + uint32_t(q4) * kFaBytes;    // its factors + flag
       for (int j = 0; j < nb; ++j, ++g) {
         const int w0 = (tb / kBlk) * kBlk + j * kBlk;
-        const int sb = g & 1, pb = g & 1;
-        float s[64];
-        ok = ok && cx.wait(B_SF0 + sb, uint32_t((g >> 1) & 1));
+        const int pb = g & 1;
+        if (j == j_pref && q_next >= 0 && hc == 0 && lane == 0)
+          prefetch_l2(p.q + (int64_t(q_next) * kHeads + q4 * 32) * kDk, 32 * kDk * 2);
+        float s[32];
+        ok = ok && cx.wait(B_SF0, uint32_t(g & 1));
         tc_fence_after();
-        const uint32_t tS = tmem + (sb ? kTS1 : kTS0) + lane_off;
-        tmem_ld32(tS, s);
-        tmem_ld32(tS + 32, s + 32);
+        {
+          float s1[32], s2[32];
+          const uint32_t tS = tmem + kTS + lane_off + 32 * hc;
+          tmem_ld32(tS, s);
+          tmem_ld32(tS + 64, s1);
+          tmem_ld32(tS + 128, s2);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = (s[c] + s1[c]) + s2[c];
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(cx.bar(B_SE0 + sb));
-        float mx = -INFINITY;
+        if (lane == 0) ptx::mbar_arrive(cx.bar(B_SE0));
+        // tokens outside [tb, te) do not take part (the block may start
+        // before the segment or run past it); the check is warp-uniform
+        const int lo = tb - w0 - 32 * hc, hi = te - w0 - 32 * hc;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (lo <= 0 && hi >= 32) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int tok = w0 + c;
-          s[c] = (tok >= tb && tok < te) ? s[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (c < lo || c >= hi) s[c] = -INFINITY;
+            m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+          }
         }
+        // the staging tile is free once the previous block's copies have read it
+        if (hc == 0 && lane == 0) bulk_wait_read0();
+        xm[hc * kHeads + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        ptx::named_bar(pair_bar, 64);
+        // scores are scaled into log2 units on the fly: the scale is positive,
+        // so the maximum of the scaled scores is the scaled maximum
+        const float mx = fmaxf(xm[row], xm[kHeads + row]) * p.scale_log2;
         float a = 1.f;
         if (j == 0) {
           mref = mx;
         } else if (mx > mref + kTau) {
-          a = exp2f(mref - mx);
+          a = ex2(mref - mx);
           mref = mx;
           l *= a;
           lf *= a;
         }
-        uint32_t pk[32];
-        float ps = 0.f, pf = 0.f;
+        uint32_t pk[16];
+        float ps2[2] = {0.f, 0.f}, pf2[2] = {0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float e0 = exp2f(s[c] - mref), e1 = exp2f(s[c + 1] - mref);
-          pf += e0 + e1;
+        for (int c = 0; c < 32; c += 2) {
+          const float e0 = ex2(fmaf(s[c], p.scale_log2, -mref)), e1 = ex2(fmaf(s[c + 1], p.scale_log2, -mref));
+          pf2[(c >> 1) & 1] += e0 + e1;
           pk[c / 2] = ptx::pack_bf16(e0, e1);
           const float2 f = ptx::unpack_bf16(pk[c / 2]);
-          ps += f.x + f.y;
+          ps2[(c >> 1) & 1] += f.x + f.y;
         }
-        l += ps;
-        lf += pf;
-        // P row into rank 1's buffer pb once PV(g-2), its previous reader, is done
-        ok = ok && cx.wait(B_PVD0 + pb, uint32_t(((g >> 1) & 1) ^ 1));
+        l += ps2[0] + ps2[1];
+        lf += pf2[0] + pf2[1];
+        // stage this half of the quarter's 32 P rows (the 128-byte swizzle
+        // depends only on row & 7, so the 4 KB tile lands in rank 1 with its
+        // final layout); half 0 also stages the rescale factors and flag
         {
-          const uint32_t prow = cx.peer_addr(cx.sbase + kOffP + uint32_t(pb) * kPBytes + uint32_t(row) * 128);
+          const uint32_t srow = stage + uint32_t(lane) * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_cluster_v4(prow + uint32_t((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                          pk[4 * c + 3]);
-          st_cluster_f32(cx.peer_addr(cx.sbase + kOffA + uint32_t(pb * kHeads + row) * 4), a);
-          const uint32_t any = __any_sync(0xffffffffu, a != 1.f) ? 1u : 0u;
-          if (lane == 0) st_cluster_u32(cx.peer_addr(cx.sbase + kOffMisc + 16 + uint32_t(pb * 4 + q4) * 4), any);
+          for (int k = 0; k < 4; ++k) {
+            const int c = 4 * hc + k;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + uint32_t((c ^ (row & 7)) << 4)),
+                         "r"(pk[4 * k]), "r"(pk[4 * k + 1]), "r"(pk[4 * k + 2]), "r"(pk[4 * k + 3])
+                         : "memory");
+          }
+          if (hc == 0) {
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(fstage + uint32_t(lane) * 4), "f"(a) : "memory");
+            const uint32_t any = __any_sync(0xffffffffu, a != 1.f) ? 1u : 0u;
+            if (lane == 0) asm volatile("st.shared.u32 [%0], %1;" ::"r"(fstage + 128), "r"(any) : "memory");
+          }
         }
-        fence_proxy_async_all();  // P is read by rank 1's tensor core (async proxy)
-        __syncwarp();
-        if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_PF0 + pb)));
+        ptx::fence_proxy_async_smem();  // staged bytes are read by the bulk copy (async proxy)
+        ptx::named_bar(pair_bar, 64);
+        // one bulk copy of the tile into P buffer pb of rank 1 once PV(g-2), its previous reader, is done
+        if (hc == 0 && lane == 0) {
+          ok = ok && cx.wait(B_PVD0 + pb, uint32_t(((g >> 1) & 1) ^ 1));
+          const uint32_t pf = cx.peer_addr(cx.bar(B_PF0 + pb));
+          arrive_expect_tx_remote_relaxed(pf, kQuarterP + kFaBytes);
+          bulk_s2s(cx.peer_addr(cx.sbase + kOffP + uint32_t(pb) * kPBytes + uint32_t(q4) * kQuarterP), stage,
+                   kQuarterP, pf);
+          bulk_s2s(cx.peer_addr(cx.sbase + kOffFa + uint32_t(pb * 4 + q4) * kFaBytes), fstage, kFaBytes, pf);
+          bulk_commit();
+        }
       }
-      // segment end: row statistics to rank 1
-      ok = ok && cx.wait(B_STE, uint32_t(stn & 1) ^ 1u);
-      const uint32_t st = cx.peer_addr(cx.sbase + kOffStats + uint32_t(row) * 4);
-      st_cluster_f32(st, mref);
-      st_cluster_f32(st + kHeads * 4, l);
-      st_cluster_f32(st + 2 * kHeads * 4, lf);
-      __syncwarp();
-      if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_STF)));
+      // segment end: the two halves' sums, then the row statistics to rank 1
+      if (hc == 1) {
+        xm[row] = l;
+        xm[kHeads + row] = lf;
+      }
+      ptx::named_bar(pair_bar, 64);
+      if (hc == 0) {
+        l += xm[row];
+        lf += xm[kHeads + row];
+        ok = ok && cx.wait(B_STE, uint32_t(stn & 1) ^ 1u);
+        const uint32_t st = cx.peer_addr(cx.sbase + kOffStats + uint32_t(row) * 4);
+        st_cluster_f32(st, mref);
+        st_cluster_f32(st + kHeads * 4, l);
+        st_cluster_f32(st + 2 * kHeads * 4, lf);
+        __syncwarp();
+        if (lane == 0) arrive_remote(cx.peer_addr(cx.bar(B_STF)));
+      }
       ++stn;
+      ptx::named_bar(pair_bar, 64);  // xm is free for the next segment
     }
+    if (hc == 0 && lane == 0) bulk_wait_read0();
     (void)ok;
-  } else if (rank == 1 && warp >= 2) {
+  } else if (rank == 1 && warp >= 2 && warp < 10) {
     // ================= rank 1 epilogue: O rescale, tails, output ================
-    const float *afac = reinterpret_cast<const float *>(smem + kOffA);
+    // Warp half hc owns O columns [256 hc, 256 hc + 256) of its quarter's rows.
     const volatile float *stats = reinterpret_cast<const volatile float *>(smem + kOffStats);
     volatile int *decision = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    const uint32_t tOh = tmem + kTO + lane_off + 256 * hc;  // this thread's row, this half's columns
+    const int col0 = 256 * hc;
     int g = 0, stn = 0;
     bool ok = true;
     for (int si = seg_lo; si < seg_hi; ++si) {
@@ -547,9 +688,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int b = sg.x, tb = sg.y, te = sg.z, wslot = sg.w;
       const int64_t orow = int64_t(b) * kHeads + row;
       if (te <= tb) {  // empty request
-        uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv);
-        for (int c = 0; c < kDv / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
-        p.lse[orow] = -INFINITY;
+        uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + col0);
+        for (int c = 0; c < 256 / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+        if (hc == 0) p.lse[orow] = -INFINITY;
         continue;
       }
       const int L = p.seqlens[b];
@@ -558,20 +699,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int w0 = (tb / kBlk) * kBlk + j * kBlk;
         const int pb = g & 1, s = g % kNst;
         ok = ok && cx.wait(B_PF0 + pb, uint32_t((g >> 1) & 1));
-        const uint32_t flag = misc[4 + pb * 4 + q4];
+        const volatile uint32_t *fa =
+            reinterpret_cast<const volatile uint32_t *>(smem + kOffFa + (pb * 4 + q4) * kFaBytes);
+        const uint32_t flag = fa[32];
         if (flag && j > 0) {
-          // the maximum of some of this warp's rows moved: scale their O rows
-          // (after PV(g-1); PV(g) waits for this warp's arrival below)
+          // the maximum of some of this quarter's rows moved: scale their O
+          // columns (after PV(g-1); PV(g) waits for this warp's arrival below)
           ok = ok && cx.wait(B_PVD0 + ((g - 1) & 1), uint32_t(((g - 1) >> 1) & 1));
           tc_fence_after();
-          const float a = afac[pb * kHeads + row];
+          const float a = __uint_as_float(fa[lane]);
           float v[32];
 #pragma unroll 1
-          for (int c = 0; c < kDv; c += 32) {
-            tmem_ld32(tmem + kTO + lane_off + c, v);
+          for (int c = 0; c < 256; c += 32) {
+            tmem_ld32(tOh + c, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= a;
-            tmem_st32(tmem + kTO + lane_off + c, reinterpret_cast<const uint32_t *>(v));
+            tmem_st32(tOh + c, reinterpret_cast<const uint32_t *>(v));
           }
         }
         if (w0 + kBlk > L) {
@@ -580,15 +723,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = ok && cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u);
           const int t_lo = max(0, min(kBlk, L - w0));
           const int nrow = kBlk - t_lo;
-          uint8_t *stage = smem + kOffRing + uint32_t(s) * kMainBytes;
+          uint8_t *stg = smem + kOffRing + uint32_t(s) * kMainBytes;
           const int pieces = 8 * nrow * 8;
-          for (int i = threadIdx.x - 64; i < pieces; i += 128) {
+          for (int i = threadIdx.x - 64; i < pieces; i += 256) {
             const int c = i / (nrow * 8), rest = i - c * (nrow * 8);
-            *reinterpret_cast<int4 *>(stage + c * kChunkBytes + (t_lo + (rest >> 3)) * 128 + (rest & 7) * 16) =
+            *reinterpret_cast<int4 *>(stg + c * kChunkBytes + (t_lo + (rest >> 3)) * 128 + (rest & 7) * 16) =
                 make_int4(0, 0, 0, 0);
           }
+          ptx::fence_proxy_async_smem();  // zeros are read by the tensor core (async proxy)
         }
-        ptx::fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(cx.bar(B_OR0 + pb));
@@ -605,40 +748,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float inv = 1.f / l;
         float v[32];
 #pragma unroll 1
-        for (int c = 0; c < kDv; c += 32) {
-          tmem_ld32(tmem + kTO + lane_off + c, v);
+        for (int c = 0; c < 256; c += 32) {
+          tmem_ld32(tOh + c, v);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) pk[i / 2] = ptx::pack_bf16(v[i] * inv, v[i + 1] * inv);
-          uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + c);
+          uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + col0 + c);
 #pragma unroll
           for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
-        p.lse[orow] = (mref + log2f(lf)) * kLn2;
+        if (hc == 0) p.lse[orow] = (mref + log2f(lf)) * kLn2;
       } else {
         // ---- split: publish the partial, the last split merges ----
         const int nsp = plan[off.nsplit + b], s0 = plan[off.slot0 + b];
-        ptx::named_bar(1, 128);  // previous use of the decision word is over
+        ptx::named_bar(1, 256);  // previous use of the decision word is over
         if (threadIdx.x == 64)
           *decision = (!*cx.abort && ld_acquire_gpu(p.item_cnt + b) == nsp - 1) ? 1 : 0;
-        ptx::named_bar(1, 128);
+        ptx::named_bar(1, 256);
         // all other splits already published: merge from TMEM without writing this one
         const bool own_tmem = *decision != 0;
         bool last = own_tmem;
         if (!own_tmem) {
+          // partial O is stored transposed, [512 columns][128 rows]: each warp
+          // store is one 128-byte line (the 32 rows of the warp, one column)
           float *ps = p.partials + int64_t(wslot) * p.slot_floats;
+          const uint64_t keep = ptx::policy_evict_last();
           float v[32];
 #pragma unroll 1
-          for (int c = 0; c < kDv; c += 32) {
-            tmem_ld32(tmem + kTO + lane_off + c, v);
-            float4 *d4 = reinterpret_cast<float4 *>(ps + row * kDv + c);
+          for (int c = 0; c < 256; c += 32) {
+            tmem_ld32(tOh + c, v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 32; ++i) st_keep(ps + (col0 + c + i) * kHeads + row, v[i], keep);
           }
-          ps[kHeads * kDv + row] = mref;
-          ps[kHeads * kDv + kHeads + row] = l;
-          ps[kHeads * kDv + 2 * kHeads + row] = lf;
-          ptx::named_bar(1, 128);
+          if (hc == 0) {
+            st_keep(ps + kHeads * kDv + row, mref, keep);
+            st_keep(ps + kHeads * kDv + kHeads + row, l, keep);
+            st_keep(ps + kHeads * kDv + 2 * kHeads + row, lf, keep);
+          }
+          ptx::named_bar(1, 256);
           if (threadIdx.x == 64) {
             int lst = 0;
             if (!*cx.abort) {
@@ -647,29 +794,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             *decision = lst;
           }
-          ptx::named_bar(1, 128);
+          ptx::named_bar(1, 256);
           last = *decision != 0;
         }
         if (last) {
           if (threadIdx.x == 64) p.item_cnt[b] = 0;  // ready for the next launch
-          // merge all splits of this row in slot order (same arithmetic whichever split merges)
+          // merge all splits of this row in slot order (same arithmetic whichever split merges);
+          // up to kU splits' statistics are loaded in one batch
+          constexpr int kU = 8;
+          float mv[kU], lv[kU], lfv[kU];
           float Mx = -INFINITY;
-          for (int s = 0; s < nsp; ++s) {
-            const float ms = (own_tmem && s0 + s == wslot)
-                                 ? mref
-                                 : __ldcg(p.partials + int64_t(s0 + s) * p.slot_floats + kHeads * kDv + row);
-            Mx = fmaxf(Mx, ms);
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            mv[u] = -INFINITY;
+            lv[u] = lfv[u] = 0.f;
+            if (u < nsp) {
+              if (own_tmem && s0 + u == wslot) {
+                mv[u] = mref;
+                lv[u] = l;
+                lfv[u] = lf;
+              } else {
+                const float *ps = p.partials + int64_t(s0 + u) * p.slot_floats + kHeads * kDv;
+                mv[u] = __ldcg(ps + row);
+                lv[u] = __ldcg(ps + kHeads + row);
+                lfv[u] = __ldcg(ps + 2 * kHeads + row);
+              }
+            }
+            Mx = fmaxf(Mx, mv[u]);
           }
+          for (int sp = kU; sp < nsp; ++sp)
+            Mx = fmaxf(Mx, (own_tmem && s0 + sp == wslot)
+                               ? mref
+                               : __ldcg(p.partials + int64_t(s0 + sp) * p.slot_floats + kHeads * kDv + row));
           const float Mu = Mx == -INFINITY ? 0.f : Mx;
           float lam = 0.f, lamf = 0.f;
-          for (int s = 0; s < nsp; ++s) {
+#pragma unroll
+          for (int u = 0; u < kU; ++u)
+            if (u < nsp) {
+              const float f = exp2f(mv[u] - Mu);
+              lam += lv[u] * f;
+              lamf += lfv[u] * f;
+            }
+          for (int sp = kU; sp < nsp; ++sp) {
             float ms, ls, lfs;
-            if (own_tmem && s0 + s == wslot) {
+            if (own_tmem && s0 + sp == wslot) {
               ms = mref;
               ls = l;
               lfs = lf;
             } else {
-              const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats + kHeads * kDv;
+              const float *ps = p.partials + int64_t(s0 + sp) * p.slot_floats + kHeads * kDv;
               ms = __ldcg(ps + row);
               ls = __ldcg(ps + kHeads + row);
               lfs = __ldcg(ps + 2 * kHeads + row);
@@ -679,42 +852,144 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             lamf += lfs * f;
           }
           const float inv = 1.f / lam;
-#pragma unroll 1
-          for (int c = 0; c < kDv; c += 32) {
-            float acc[32];
+          const int own = wslot - s0;
+          if (si == seg_hi - 1 && nsp <= 63) {
+            // Fast path (the merge of a worker's last segment, the usual case:
+            // the other splits finished long before): the KV ring is idle, so
+            // the other splits' partial O stream into it by TMA, per warp 4
+            // slots of 32 rows x 32 columns; this split's O comes from TMEM, and
+            // the bf16 result leaves through two 4 KB staging tiles by TMA.
+            constexpr int kMs = 4;
+            const int n_o = nsp - 1, total = 8 * n_o;  // items: (32-column chunk, other split)
+            const int wi = warp - 2;                    // 0..7
+            const uint32_t mring = cx.sbase + kOffRing + uint32_t(wi) * (kMs * 4096 + 8192);
+            const uint32_t ostage = mring + kMs * 4096;
+            const uint32_t mbar = cx.sbase + kOffP + uint32_t(wi) * 32;  // P buffers are idle too
+            float *fw = reinterpret_cast<float *>(smem + kOffP + 256);  // per-split weights [split][row]
+            const uint64_t pol = ptx::policy_evict_first();
+            if (hc == 0) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            for (int s = 0; s < nsp; ++s) {
-              float v[32];
-              float ms;
-              if (own_tmem && s0 + s == wslot) {
-                tmem_ld32(tmem + kTO + lane_off + c, v);
-                ms = mref;
-              } else {
-                const float *ps = p.partials + int64_t(s0 + s) * p.slot_floats;
-                const float4 *src = reinterpret_cast<const float4 *>(ps + row * kDv + c);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float4 x = __ldcg(src + i);
-                  v[4 * i] = x.x;
-                  v[4 * i + 1] = x.y;
-                  v[4 * i + 2] = x.z;
-                  v[4 * i + 3] = x.w;
-                }
-                ms = __ldcg(ps + kHeads * kDv + row);
-              }
-              const float f = exp2f(ms - Mu);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i] += v[i] * f;
+              for (int u = 0; u < kU; ++u)
+                if (u < nsp) fw[u * kHeads + row] = exp2f(mv[u] - Mu);
+              for (int sp = kU; sp < nsp; ++sp)
+                fw[sp * kHeads + row] = exp2f(
+                    (sp == own ? mref : __ldcg(p.partials + int64_t(s0 + sp) * p.slot_floats + kHeads * kDv + row)) -
+                    Mu);
             }
-            uint32_t pk[16];
+            if (lane == 0) {
+              for (int k = 0; k < kMs; ++k) ptx::mbar_init(mbar + 8 * k, 1);
+              ptx::fence_mbar_init();
+            }
+            ptx::named_bar(1, 256);  // weights visible to both halves
+            auto issue = [&](int i) {
+              const int slot = i % kMs, c = i / n_o, k = i % n_o, sp = k + (k >= own ? 1 : 0);
+              ptx::mbar_arrive_expect_tx(mbar + 8 * slot, 4096);
+              tma3(mring + slot * 4096, &tpart, mbar + 8 * slot, q4 * 32, col0 + c * 32, s0 + sp, pol);
+            };
+            int issued = 0;
+            if (lane == 0)
+              for (; issued < min(kMs, total); ++issued) issue(issued);
+            int it = 0;
+            bool mok = true;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {  // 32-column chunks of this half
+              float acc[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) pk[i / 2] = ptx::pack_bf16(acc[i] * inv, acc[i + 1] * inv);
-            uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + c);
+              for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+#pragma unroll 1
+              for (int sp = 0; sp < nsp; ++sp) {
+                float v[32];
+                if (sp == own) {
+                  tmem_ld32(tOh + c * 32, v);
+                } else {
+                  const int slot = it % kMs;
+                  if (mok && !ptx::mbar_wait(mbar + 8 * slot, uint32_t(it / kMs) & 1u, cx.abort, kWaitCycles)) {
+                    mok = false;
+                    if (lane == 0 && !*cx.abort) {
+                      *cx.abort = 1;
+                      atomicOr(p.err, SKD_DEVERR_TIMEOUT);
+                    }
+                  }
+                  // a box holds 32 columns x 32 rows (128 B per column); the
+                  // 16-byte chunk k (rows 4k..4k+3) of column j sits at k ^ (j & 7)
+                  const uint32_t rb = mring + slot * 4096 + uint32_t(lane & 3) * 4;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                  for (int jj = 0; jj < 32; ++jj)
+                    asm volatile("ld.shared.f32 %0, [%1];"
+                                 : "=f"(v[jj])
+                                 : "r"(rb + uint32_t(jj) * 128 + uint32_t((((lane >> 2) ^ (jj & 7)) << 4)))
+                                 : "memory");
+                  __syncwarp();  // the slot is read before it is refilled
+                  if (lane == 0 && issued < total && mok) issue(issued++);
+                  ++it;
+                }
+                const float f = fw[sp * kHeads + row];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] += v[i] * f;
+              }
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) pk[i / 2] = ptx::pack_bf16(acc[i] * inv, acc[i + 1] * inv);
+              // a 64-column output tile is two chunks; tile (c/2) & 1 is free
+              // once the store issued two tiles ago has read it
+              if ((c & 1) == 0) {
+                if (lane == 0 && c >= 4) bulk_wait_read1();
+                __syncwarp();
+              }
+              const uint32_t ot = ostage + uint32_t((c >> 1) & 1) * 4096 + uint32_t(lane) * 128;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int cc = 4 * (c & 1) + k;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ot + uint32_t((cc ^ (lane & 7)) << 4)),
+                             "r"(pk[4 * k]), "r"(pk[4 * k + 1]), "r"(pk[4 * k + 2]), "r"(pk[4 * k + 3])
+                             : "memory");
+              }
+              if (c & 1) {
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store2(&tout, ostage + uint32_t((c >> 1) & 1) * 4096, col0 + (c >> 1) * 64, b * kHeads + q4 * 32);
+                  bulk_commit();
+                }
+              }
+            }
+            if (lane == 0) bulk_wait0();
+            // after a give-up, the loads still in flight land before the CTA leaves
+            if (lane == 0)
+              for (int i = it; i < issued; ++i)
+                ptx::mbar_wait(mbar + 8 * (i % kMs), uint32_t(i / kMs) & 1u, nullptr, kWaitCycles);
+            __syncwarp();
+          } else {
+#pragma unroll 1
+            for (int c = 0; c < 256; c += 32) {
+              float acc[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+              for (int sp = 0; sp < nsp; ++sp) {
+                float v[32];
+                float ms;
+                if (sp == own) {
+                  tmem_ld32(tOh + c, v);
+                  ms = mref;
+                } else {
+                  const float *ps = p.partials + int64_t(s0 + sp) * p.slot_floats;
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) v[i] = __ldcg(ps + (col0 + c + i) * kHeads + row);
+                  ms = __ldcg(ps + kHeads * kDv + row);
+                }
+                const float f = exp2f(ms - Mu);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] += v[i] * f;
+              }
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) pk[i / 2] = ptx::pack_bf16(acc[i] * inv, acc[i + 1] * inv);
+              uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + col0 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
-          p.lse[orow] = (Mx + log2f(lamf)) * kLn2;
+          if (hc == 0) p.lse[orow] = (Mx + log2f(lamf)) * kLn2;
         }
       }
       tc_fence_before();  // O reads done before the next segment's first PV overwrites it
@@ -749,7 +1024,7 @@ int launch_mla(const DecodeArgs &a) {
   const skd_shape_t &s = a.shape;
   if (s.page_size % kBlk != 0) return SKD_EUNSUPPORTED;  // 64-token blocks must not straddle pages
   // latent cache viewed as {64 columns, rows (page*P + slot), 9 column chunks}
-  CUtensorMap tmain, trope;
+  CUtensorMap tmain, trope, tpart, tout;
   const cuuint64_t gk[3] = {64, cuuint64_t(s.num_pages) * s.page_size, 9};
   const cuuint64_t sk[2] = {cuuint64_t(s.v_row_stride) * 2, 128};
   const cuuint32_t es[3] = {1, 1, 1};
@@ -759,6 +1034,23 @@ int launch_mla(const DecodeArgs &a) {
       encode_tiled(&trope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k), gk, sk, brope, es,
                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return SKD_EINVAL;
+  // partial-state slots (O stored transposed) viewed as {128 rows, 512 columns, slots} fp32, boxes of 32 x 32
+  {
+    uint8_t *ws = static_cast<uint8_t *>(a.ws);
+    const cuuint64_t gp[3] = {cuuint64_t(kHeads), cuuint64_t(kDv), cuuint64_t(std::max<int64_t>(a.wl.slots, 1))};
+    const cuuint64_t spb[2] = {cuuint64_t(kHeads) * 4, cuuint64_t(a.wl.slot_floats) * 4};
+    const cuuint32_t bp[3] = {32, 32, 1};
+    if (encode_tiled(&tpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws + a.wl.partials, gp, spb, bp, es,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return SKD_EINVAL;
+    // output rows {512 columns, batch*128 rows} bf16, boxes of 64 x 32
+    const cuuint64_t go[2] = {cuuint64_t(kDv), cuuint64_t(s.batch) * kHeads};
+    const cuuint64_t so[1] = {cuuint64_t(kDv) * 2};
+    const cuuint32_t bo[2] = {64, 32};
+    if (encode_tiled(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, go, so, bo, es,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return SKD_EINVAL;
+  }
   Params p;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.page_table = a.page_table;
@@ -785,7 +1077,7 @@ int launch_mla(const DecodeArgs &a) {
       return SKD_ECUDA;
     attr_set = true;
   }
-  mla_decode_kernel<<<2 * a.n_ctas, kThreads, kSmemBytes, a.stream>>>(tmain, trope, p);
+  mla_decode_kernel<<<2 * a.n_ctas, kThreads, kSmemBytes, a.stream>>>(tmain, trope, tpart, tout, p);
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

@@ -66,10 +66,10 @@ __device__ int block_exclusive_scan(int32_t *a, int len, int32_t *warp_sums, int
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
-    plan_device_kernel(const int32_t *__restrict__ seqlens, int batch, int ngrp, int n,
+    plan_device_kernel(const int32_t *__restrict__ seqlens, int batch, int ngrp, int n, int seg_cost,
                        int32_t *__restrict__ plan) {
   extern __shared__ int32_t sm[];
-  int32_t *req_pref = sm;                 // [batch + 1] granule prefix per request
+  int32_t *req_pref = sm;                 // [batch + 1] virtual-granule prefix per request
   int32_t *cnt = req_pref + batch + 1;    // [n + 1] segments per CTA -> offsets
   int32_t *first = cnt + n + 1;           // [n] smallest item of each CTA
   __shared__ int32_t warp_sums[33];
@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   for (int b = tid; b < batch; b += kPlanThreads) {
     const int L = seqlens[b];
     if (L < 0) atomicOr(&err, SKD_DEVERR_SEQLEN);
-    req_pref[b] = L > 0 ? (L + kGranule - 1) / kGranule : 0;
+    // each of the request's ngrp items: its segment cost, then its granules
+    req_pref[b] = L > 0 ? (L + kGranule - 1) / kGranule + seg_cost : 0;
   }
   for (int c = tid; c <= n; c += kPlanThreads) cnt[c] = 0;
   for (int c = tid; c < n; c += kPlanThreads) first[c] = 0x7fffffff;
@@ -116,8 +117,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   // pass 1: per item, the CTAs it touches; count segments per CTA
   for (int64_t i = tid; i < items; i += kPlanThreads) {
     const int b = int(i / ngrp), h = int(i - int64_t(b) * ngrp);
-    const int64_t g = req_pref[b + 1] - req_pref[b];
-    const int64_t s = int64_t(ngrp) * req_pref[b] + h * g, e = s + g;
+    const int64_t gv = req_pref[b + 1] - req_pref[b];  // virtual length of each item of b
+    const int64_t g = gv > 0 ? gv - seg_cost : 0;
+    const int64_t s = int64_t(ngrp) * req_pref[b] + h * gv + (gv - g), e = s + g;
     int ns = 0;
     if (g == 0) {
       const int64_t c = cta_of(s, total, n);
@@ -149,8 +151,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   for (int64_t i = tid; i < items; i += kPlanThreads) {
     const int b = int(i / ngrp), h = int(i - int64_t(b) * ngrp);
     const int L = seqlens[b];
-    const int64_t g = req_pref[b + 1] - req_pref[b];
-    const int64_t s = int64_t(ngrp) * req_pref[b] + h * g, e = s + g;
+    const int64_t gv = req_pref[b + 1] - req_pref[b];
+    const int64_t g = gv > 0 ? gv - seg_cost : 0;
+    const int64_t s = int64_t(ngrp) * req_pref[b] + h * gv + (gv - g), e = s + g;
     const int ns = nsplit[i];
     const int sl0 = ns > 1 ? slot0[i] : -1;
     if (g == 0) {
@@ -190,20 +193,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     plan[PH_MODE] = SKD_PLAN_STREAMK;
     plan[PH_SEGCAP] = int(cap);
     plan[PH_ERR] = 0;
+    plan[PH_SEGCOST] = seg_cost;
   }
 }
 
 }  // namespace
 
-int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n, int32_t *plan,
+int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n, int seg_cost, int32_t *plan,
                        cudaStream_t stream) {
+  if (seg_cost < 0 || seg_cost > kMaxSegCost) return SKD_EINVAL;
   const size_t smem = size_t(batch + 1 + 2 * (n + 1)) * 4;
   if (smem > 200 * 1024) return SKD_EUNSUPPORTED;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(plan_device_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return SKD_ECUDA;
-  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seqlens, batch, ngrp, n, plan);
+  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seqlens, batch, ngrp, n, seg_cost, plan);
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

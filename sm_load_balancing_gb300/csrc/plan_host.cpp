@@ -9,6 +9,13 @@
 // Work item i = b*NGRP + g (kv-head group g) carries ceil(L_b / 16) granules; CTA c receives the
 // granule range [floor(c*G/n), floor((c+1)*G/n)) of the items laid end to end,
 // cut at item boundaries. A single linear sweep, O(items + n).
+//
+// Optional segment cost (an extension beyond the pages): every non-empty item
+// is preceded by `seg_cost` virtual granules that carry no tokens, standing for
+// the fixed work a CTA spends per segment (loading the item's queries, writing
+// its output or partial state). The equal split then runs over the virtual
+// total, so a CTA that crosses many item boundaries receives fewer tokens.
+// seg_cost = 0 is the plain split.
 #include <string.h>
 
 #include <vector>
@@ -21,11 +28,12 @@ namespace skd {
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, int n, int mode,
-                    void *plan_out, size_t plan_bytes) {
+                    int seg_cost, void *plan_out, size_t plan_bytes) {
   if (!seqlens && batch > 0) return SKD_EINVAL;
   if (!plan_out || batch < 0 || ngrp <= 0 || n <= 0) return SKD_EINVAL;
   if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
   if (mode != SKD_PLAN_STREAMK && mode != SKD_PLAN_ROUND_ROBIN) return SKD_EINVAL;
+  if (seg_cost < 0 || seg_cost > kMaxSegCost || (seg_cost > 0 && mode != SKD_PLAN_STREAMK)) return SKD_EINVAL;
   const PlanOffsets off = plan_offsets(batch, ngrp, n);
   if (plan_bytes < size_t(off.words) * 4) return SKD_EPLAN;
   for (int b = 0; b < batch; ++b)
@@ -40,8 +48,11 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
   int32_t *nsplit = w + off.nsplit;
   int32_t *slot0 = w + off.slot0;
 
-  int64_t total = 0;
-  for (int b = 0; b < batch; ++b) total += int64_t(ngrp) * ceil_div(seqlens[b], kGranule);
+  int64_t total = 0;  // virtual granules
+  for (int b = 0; b < batch; ++b) {
+    const int64_t g = ceil_div(seqlens[b], kGranule);
+    total += int64_t(ngrp) * (g + (g > 0 ? seg_cost : 0));
+  }
   if (total > INT32_MAX) return SKD_EPLAN;
 
   int64_t nseg = 0;
@@ -68,7 +79,8 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
     for (int64_t i = 0; i < items; ++i) {
       const int64_t L = seqlens[i / ngrp];
       const int64_t g = ceil_div(L, kGranule);
-      const int64_t s = pos, e = pos + g;
+      // token granules of the item occupy [s, e) after its virtual segment cost
+      const int64_t s = pos + (g > 0 ? seg_cost : 0), e = s + g;
       pos = e;
       // first CTA whose chunk ends after s (the last CTA if none)
       int64_t cs = c;
@@ -129,6 +141,7 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
   w[PH_MODE] = mode;
   w[PH_SEGCAP] = int32_t(cap);
   w[PH_ERR] = 0;
+  w[PH_SEGCOST] = seg_cost;
   return SKD_OK;
 }
 

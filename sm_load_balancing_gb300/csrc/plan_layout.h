@@ -29,6 +29,7 @@ SKD_HD inline int head_group(int hkv) {
 
 constexpr int32_t kPlanMagic = 0x534B4431;  // "SKD1"
 constexpr int kGranule = 16;
+constexpr int kMaxSegCost = 1 << 16;  // granules
 
 enum PlanHeader : int {
   PH_MAGIC = 0,
@@ -43,6 +44,7 @@ enum PlanHeader : int {
   PH_MODE = 9,
   PH_SEGCAP = 10,
   PH_ERR = 11,  // device planner's error bits (SKD_DEVERR_*), 0 from the host planner
+  PH_SEGCOST = 12,  // virtual granules charged per non-empty item (0: plain split)
   PH_WORDS = 16
 };
 

@@ -28,11 +28,14 @@ class Dev:
         self.sl = torch.from_numpy(w.seqlens).cuda()
         self.shape = skd.make_shape(self.q, self.k, self.v, self.pt, scale=w.scale, causal=w.causal)
 
-    def run(self, n_ctas=None, mode="streamk", plan=None, ws=None, out=None, lse=None):
+    def run(self, n_ctas=None, mode="streamk", plan=None, ws=None, out=None, lse=None, seg_cost=None):
         skd = self.skd
         n = skd.default_ctas(self.shape) if n_ctas is None else n_ctas
         if plan is None:
-            plan = skd.plan(self.w.seqlens, self.shape.num_kv_heads, self.w.page_size, n, mode).cuda()
+            if seg_cost is None:
+                seg_cost = skd.default_seg_cost(self.shape) if mode == "streamk" else 0
+            plan = skd.plan(self.w.seqlens, self.shape.num_kv_heads, self.w.page_size, n, mode,
+                            seg_cost=seg_cost).cuda()
         if ws is None:
             ws = skd.workspace(self.shape, n)
         o, l = skd.decode_attention(self.q, self.k, self.v, self.pt, self.sl, plan, ws,

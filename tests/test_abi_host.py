@@ -46,11 +46,15 @@ def test_every_declared_symbol_is_exported(N):
     assert lib.skd_abi_version() == 1
 
 
-def _host_plan(N, seqlens, hkv, n, mode=0, page_size=16):
+def _host_plan(N, seqlens, hkv, n, mode=0, page_size=16, seg_cost=None):
     sl = np.ascontiguousarray(seqlens, dtype=np.int32)
     nb = N.lib().skd_plan_bytes(len(sl), hkv, n)
     buf = np.zeros(nb // 4, dtype=np.int32)
-    st = N.lib().skd_decode_plan(sl.ctypes.data, len(sl), hkv, page_size, n, mode, buf.ctypes.data, nb)
+    if seg_cost is None:
+        st = N.lib().skd_decode_plan(sl.ctypes.data, len(sl), hkv, page_size, n, mode, buf.ctypes.data, nb)
+    else:
+        st = N.lib().skd_decode_plan_weighted(sl.ctypes.data, len(sl), hkv, page_size, n, seg_cost,
+                                              buf.ctypes.data, nb)
     return st, buf
 
 
@@ -61,11 +65,11 @@ def head_groups(hkv):
     return hkv // hg
 
 
-def _check_against_oracle(N, seqlens, hkv, n):
-    st, buf = _host_plan(N, seqlens, hkv, n)
+def _check_against_oracle(N, seqlens, hkv, n, seg_cost=None):
+    st, buf = _host_plan(N, seqlens, hkv, n, seg_cost=seg_cost)
     assert st == 0
     p = PD.decode(buf)
-    ref = S.streamk_split(seqlens, head_groups(hkv), n, granule=16)
+    ref = S.streamk_split(seqlens, head_groups(hkv), n, granule=16, seg_cost=seg_cost or 0)
     got = [[(i, tb, te) for i, tb, te, _ in segs] for segs in p["segments"]]
     assert got == ref["segments"]
     assert p["total"] == ref["total_granules"]
@@ -111,6 +115,50 @@ def test_host_planner_on_named_workloads(N, name, n):
     p = _check_against_oracle(N, sl.tolist(), hkv, n)
     per = [sum(-(-(te - tb) // 16) for _, tb, te, _ in segs) for segs in p["segments"]]
     assert max(per) - min(per) <= 1
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_weighted_planner_equals_definition(N, seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 12))
+    hkv = int(rng.choice([1, 2, 8, 12]))
+    n = int(rng.choice([1, 2, 5, 13, 76, 148]))
+    seg_cost = int(rng.choice([0, 1, 7, 40, 1000]))
+    seqlens = [int(x) for x in rng.integers(0, 3000, size=B)]
+    if seed % 4 == 0:
+        seqlens[int(rng.integers(0, B))] = 0
+    p = _check_against_oracle(N, seqlens, hkv, n, seg_cost=seg_cost)
+    assert p["total"] == sum(head_groups(hkv) * (-(-L // 16) + (seg_cost if L else 0)) for L in seqlens)
+    # every token granule is planned exactly once
+    for i in range(len(seqlens) * head_groups(hkv)):
+        L = seqlens[i // head_groups(hkv)]
+        pieces = sorted((tb, te) for segs in p["segments"] for it, tb, te, _ in segs if it == i)
+        if L == 0:
+            assert pieces == [(0, 0)]
+        else:
+            assert pieces[0][0] == 0 and pieces[-1][1] == L
+            assert all(a[1] == b[0] for a, b in zip(pieces, pieces[1:]))
+
+
+def test_weighted_planner_zero_cost_is_plain_split(N):
+    sl = W.draw_seqlens("mla_absorbed").tolist()
+    _, a = _host_plan(N, sl, 1, 76)
+    _, b = _host_plan(N, sl, 1, 76, seg_cost=0)
+    assert np.array_equal(a, b)
+
+
+def test_weighted_planner_gives_fewer_tokens_to_boundary_heavy_ctas(N):
+    # one CTA range crosses many short requests: the cost moves tokens away from it
+    sl = [4096] * 3 + [64] * 40 + [4096] * 3
+    st, buf = _host_plan(N, sl, 1, 8, seg_cost=32)
+    assert st == 0
+    p = PD.decode(buf)
+    toks = [sum(te - tb for _, tb, te, _ in segs) for segs in p["segments"]]
+    nseg = [len(segs) for segs in p["segments"]]
+    heavy = int(np.argmax(nseg))
+    assert nseg[heavy] > 10 and toks[heavy] < min(t for c, t in enumerate(toks) if nseg[c] <= 2)
+    assert _host_plan(N, sl, 1, 8, seg_cost=-1)[0] == N.SKD_EINVAL
+    assert _host_plan(N, sl, 1, 8, seg_cost=70000)[0] == N.SKD_EINVAL
 
 
 def test_head_group_rule():

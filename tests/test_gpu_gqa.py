@@ -139,6 +139,19 @@ def test_device_planner_matches_host_planner():
         host = skd.plan(sl, hkv, 64, 152)
         dev = skd.plan_device(torch.from_numpy(sl).cuda(), hkv, 64, 152)
         assert torch.equal(host, dev.cpu())
+    # the weighted split, same bytes on both sides
+    for trial in range(12):
+        B = int(rng.integers(1, 70))
+        hkv = int(rng.choice([1, 2, 8]))
+        n = int(rng.choice([1, 76, 152]))
+        c = int(rng.choice([1, 40, 999]))
+        sl = rng.integers(0, 9000, size=B).astype(np.int32)
+        if trial % 3 == 0:
+            sl[rng.integers(0, B)] = 0
+        host = skd.plan(sl, hkv, 16, n, seg_cost=c)
+        dev = skd.plan_device(torch.from_numpy(sl).cuda(), hkv, 16, n, seg_cost=c)
+        torch.cuda.synchronize()
+        assert torch.equal(host, dev.cpu()), (trial, B, hkv, n, c)
 
 
 def test_device_plan_drives_the_kernel():
