@@ -164,6 +164,128 @@ __device__ void merge_head(const Params &p, int h, int base, int n, int stride, 
   }
 }
 
+// The same merge for a CTA's last segment, when its KV ring is idle: whole
+// partial-state slots (all HG heads of one split, contiguous) stream through
+// the ring as one large bulk copy each, several slots in flight, and every
+// consumer warp folds its head's block of each slot in split order with a
+// running maximum. One thread of warp 0 issues the copies and refills a buffer
+// once all HG warps have released it. `uses` numbers the buffer fills across
+// calls (a fold followed by the final merge) so that barrier phases continue.
+template <int D>
+__device__ __noinline__ bool merge_slots_staged(const Params &p, int h, int HG, int base, int n, int stride,
+                                               bool final_out, int b, int head, int lane, uint32_t ring,
+                                               uint32_t ring_bytes, const volatile int *abort, int &uses) {
+  constexpr int C4 = D / 32;
+  const int rows = p.rows;
+  const uint32_t sb = uint32_t(p.slot_floats) * 4;
+  const int nbuf = min(6, int((ring_bytes - 128) / sb));
+  const uint32_t full = ring + ring_bytes - 128, empty = full + 64;
+  // lane (rg, cl) handles row 4g + rg and the float4 columns c * 8 + cl, so the
+  // eight lanes of a row read 128 contiguous bytes (no bank conflicts)
+  const int rg = lane >> 3, cl = lane & 7;
+  const int RG = (rows + 3) >> 2;  // row groups of 4 (rows <= 16)
+  const bool issuer = h == 0 && lane == 0;
+  if (uses == 0 && issuer) {
+    for (int k = 0; k < nbuf; ++k) {
+      ptx::mbar_init(full + 8 * k, 1);
+      ptx::mbar_init(empty + 8 * k, uint32_t(HG));
+    }
+    ptx::fence_mbar_init();
+  }
+  // the copies read partial states through the async proxy: order this CTA's
+  // own earlier stores to them (a folded run) and the acquired ones of other CTAs
+  ptx::fence_proxy_async_global();
+  ptx::named_bar(1, HG * 32);
+  const int u0 = uses;
+  auto fill = [&](int s) {
+    const int u = u0 + s, k = u % nbuf;
+    ptx::mbar_arrive_expect_tx(full + 8 * k, sb);
+    ptx::bulk_load(ring + k * sb, p.partials + int64_t(base + s * stride) * p.slot_floats, sb, full + 8 * k);
+  };
+  int issued = 0;
+  if (issuer)
+    for (; issued < min(nbuf, n); ++issued) fill(issued);
+  float M[4], lam[4], lamf[4];
+  float4 acc[4][C4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    M[k] = -INFINITY;
+    lam[k] = lamf[k] = 0.f;
+#pragma unroll
+    for (int c = 0; c < C4; ++c) acc[k][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  bool ok = true;
+  for (int s = 0; s < n; ++s) {
+    const int u = u0 + s, k = u % nbuf;
+    if (ok && !ptx::mbar_wait(full + 8 * k, uint32_t(u / nbuf) & 1u, abort, kWaitCycles)) ok = false;
+    const float *bs =
+        reinterpret_cast<const float *>(__cvta_shared_to_generic(ring + k * sb)) + int64_t(h) * p.head_floats;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int r = 4 * g + rg;
+      if (g < RG && r < rows) {
+        const float mv = bs[rows * D + r];
+        const float Mn = fmaxf(M[g], mv);
+        const float Mu = Mn == -INFINITY ? 0.f : Mn;
+        const float sc = exp2f(M[g] - Mu), f = exp2f(mv - Mu);
+        lam[g] = lam[g] * sc + bs[rows * D + rows + r] * f;
+        lamf[g] = lamf[g] * sc + bs[rows * D + 2 * rows + r] * f;
+        const float4 *o = reinterpret_cast<const float4 *>(bs + r * D);
+#pragma unroll
+        for (int c = 0; c < C4; ++c) {
+          const float4 v = o[c * 8 + cl];
+          acc[g][c].x = acc[g][c].x * sc + v.x * f;
+          acc[g][c].y = acc[g][c].y * sc + v.y * f;
+          acc[g][c].z = acc[g][c].z * sc + v.z * f;
+          acc[g][c].w = acc[g][c].w * sc + v.w * f;
+        }
+        M[g] = Mn;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(empty + 8 * k);
+    if (issuer && ok && issued < n) {
+      // the buffer of split s is refilled with split s + nbuf once every warp released it
+      if (!ptx::mbar_wait(empty + 8 * k, uint32_t(u / nbuf) & 1u, abort, kWaitCycles)) ok = false;
+      if (ok) fill(issued++);
+    }
+  }
+  // after a give-up, the copies still in flight land before the ring is reused
+  if (!ok && issuer) {
+    atomicOr(p.err, SKD_DEVERR_TIMEOUT);
+    for (int s = 0; s < issued; ++s)
+      ptx::mbar_wait(full + 8 * ((u0 + s) % nbuf), uint32_t((u0 + s) / nbuf) & 1u, nullptr, kWaitCycles);
+  }
+  uses = u0 + n;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int r = 4 * g + rg;
+    if (g >= RG || r >= rows) continue;
+    if (final_out) {
+      const int t = r / p.G;
+      const int64_t orow = (int64_t(b) * p.T + t) * p.Hq + int64_t(head) * p.G + (r - t * p.G);
+      const float inv = 1.f / lam[g];
+      uint2 *dst = reinterpret_cast<uint2 *>(p.out + orow * D);
+#pragma unroll
+      for (int c = 0; c < C4; ++c)
+        dst[c * 8 + cl] = make_uint2(ptx::pack_bf16(acc[g][c].x * inv, acc[g][c].y * inv),
+                                     ptx::pack_bf16(acc[g][c].z * inv, acc[g][c].w * inv));
+      if (cl == 0) p.lse[orow] = (M[g] + log2f(lamf[g])) * kLn2;
+    } else {
+      float *pd = p.partials + int64_t(base) * p.slot_floats + h * p.head_floats;
+      float4 *o = reinterpret_cast<float4 *>(pd + r * D);
+#pragma unroll
+      for (int c = 0; c < C4; ++c) o[c * 8 + cl] = acc[g][c];
+      if (cl == 0) {
+        pd[rows * D + r] = M[g];
+        pd[rows * D + rows + r] = lam[g];
+        pd[rows * D + 2 * rows + r] = lamf[g];
+      }
+    }
+  }
+  return ok;
+}
+
 template <int D>
 __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -587,8 +709,16 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
       }
       ptx::named_bar(1, cthreads);
       int last = *last_flag;
+      // merges of many splits in this CTA's last segment go through its idle KV ring
+      const uint32_t ring_bytes = uint32_t(p.nst * p.stage_bytes);
+      const bool can_stage = si == seg_hi - 1 && ring_bytes >= 2 * uint32_t(p.slot_floats) * 4 + 128;
+      int staged_uses = 0;
       auto merge = [&](int mbase, int mn, int mstride, bool fin) {
-        merge_head<D>(p, h, mbase, mn, mstride, fin, b, head, lane);
+        if (can_stage && mn >= 8)
+          merge_slots_staged<D>(p, h, HG, mbase, mn, mstride, fin, b, head, lane, sbase, ring_bytes, abort_flag,
+                                staged_uses);
+        else
+          merge_head<D>(p, h, mbase, mn, mstride, fin, b, head, lane);
       };
       if (last == 1) {  // fold this run of kFan splits into its first slot
         const int gsz = min(kFan, nsp - k * kFan);

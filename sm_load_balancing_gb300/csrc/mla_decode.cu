@@ -913,6 +913,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma3(mring + slot * 4096, &tpart, mbar + 8 * slot, q4 * 32, col0 + c * 32, s0 + sp, pol);
             };
             int issued = 0;
+            // the TMA reads partials published by other CTAs (acquired above)
+            // through the async proxy
+            if (lane == 0) ptx::fence_proxy_async_global();
             if (lane == 0)
               for (; issued < min(kMs, total); ++issued) issue(issued);
             int it = 0;
