@@ -53,6 +53,9 @@ def _args():
                     help="target CPU time of the oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--launch-study", action="store_true",
+                    help="also time one step = device planner + attention: eager vs CUDA graph, "
+                         "with and without programmatic dependent launch")
     return ap.parse_args()
 
 
@@ -83,6 +86,50 @@ def _measured_hbm_peak():
         return None
     v = find(d)
     return (v, "measured (MEASURED_PEAKS.json hbm_gbs)") if v else (FALLBACK_HBM_GBS, "fallback")
+
+
+def _launch_study(skd, q, k, v, pt, sl, w, shape, n, seg_cost, ws, out, lse, a):
+    """Per-step time of device planner + attention, four ways: eager launches or
+    one CUDA graph replay, each with programmatic dependent launch on or off.
+    The difference to the kernel time alone is what launching costs per step."""
+    import torch
+    hkv = shape.num_kv_heads
+    plan = skd.plan_device(sl, hkv, w.page_size, n, seg_cost=seg_cost)
+    res = {}
+    steps = max(50, min(a.steps, 500))
+    for pdl in (False, True):
+        skd.set_pdl(pdl)
+
+        def step():
+            skd.plan_device(sl, hkv, w.page_size, n, out=plan, seg_cost=seg_cost)
+            skd.decode_attention(q, k, v, pt, sl, plan, ws, scale=w.scale, causal=w.causal, n_ctas=n,
+                                 out=out, lse=lse, shape=shape)
+
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=st):
+            step()
+        torch.cuda.current_stream().wait_stream(st)
+        for name, fn in (("eager", step), ("graph", g.replay)):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            res[f"{name}{'_pdl' if pdl else ''}_us"] = e0.elapsed_time(e1) / steps * 1e3
+    skd.set_pdl(True)
+    if skd.read_error(ws) != 0:
+        raise RuntimeError(f"device error word {skd.read_error(ws)}")
+    res["steps"] = steps
+    return res
 
 
 def _traffic(kind, workload):
@@ -296,6 +343,7 @@ def run_ours(a):
     err = skd.read_error(ws)
     if err != 0:
         raise RuntimeError(f"device error word {err}")
+    launch = _launch_study(skd, q, k, v, pt, sl, w, shape, n, seg_cost, ws, out, lse, a) if a.launch_study else None
 
     if world > 1:
         import torch.distributed as dist
@@ -375,6 +423,8 @@ def run_ours(a):
         "gpu_launches": a.steps,
         "clocks": ck,
     }
+    if launch is not None:
+        line["launch"] = launch
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         try:
             bps, cores, desc, dt = _cpu_oracle_sample(w, a.cpu_seconds)

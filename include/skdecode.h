@@ -158,6 +158,16 @@ int skd_decode_plan_weighted_device(const int32_t *seqlens_dev, int batch, int n
                                     int n_ctas, int seg_cost, void *plan_dev, size_t plan_bytes,
                                     void *stream);
 
+/* Launch option (process-wide, default on): launch the attention kernel with
+ * programmatic dependent launch, so that it can be scheduled while the
+ * previous kernel of the stream (typically skd_decode_plan_device, which
+ * signals its dependents as soon as it starts) is still running; the kernel
+ * waits for that grid to complete before reading any input, so results do not
+ * change. This is the launch-overlap idea of "GPU Kernel、异步 Launch、Stream 与
+ * 融合 Kernel 全解" (section 7, launch gaps in a decode step). 0 turns it off.
+ * Always SKD_OK. */
+int skd_set_pdl(int enable);
+
 /* ---- workspace --------------------------------------------------------- */
 
 /* Bytes of the workspace skd_decode_attention needs for this shape and grid:

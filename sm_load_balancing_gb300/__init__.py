@@ -23,7 +23,7 @@ from ._native import (SKD_DEVERR_PAGE, SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN,
                       SKD_DEVERR_TIMEOUT, SKD_GRANULE, SkdError)
 
 __all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention", "read_error",
-           "sm_count", "default_ctas", "default_seg_cost", "make_shape", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
+           "sm_count", "default_ctas", "default_seg_cost", "make_shape", "set_pdl", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
            "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT"]
 
 _MODES = {"streamk": N.SKD_PLAN_STREAMK, "round_robin": N.SKD_PLAN_ROUND_ROBIN}
@@ -171,6 +171,13 @@ def decode_attention(q, k_pages, v_pages, page_table, seqlens, plan_dev, ws, *, 
         seqlens.data_ptr(), plan_dev.data_ptr(), n, ws.data_ptr(), ws.numel(), out.data_ptr(),
         lse.data_ptr(), _stream_ptr(stream)))
     return out, lse
+
+
+def set_pdl(enable: bool) -> None:
+    """Launch the attention kernel with programmatic dependent launch (default
+    on): it may be scheduled while the previous kernel of the stream, e.g. the
+    device planner, is still running, and waits for it before reading inputs."""
+    N.check("skd_set_pdl", N.lib().skd_set_pdl(1 if enable else 0))
 
 
 def read_error(ws: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -46,6 +46,7 @@ SIGNATURES = {
                                       _vp, _c_size, _vp, _vp, _vp]),
     "skd_read_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "skd_trace_enable": (_c_int, [_vp, _c_size]),
+    "skd_set_pdl": (_c_int, [_c_int]),
     "skd_decode_attention_noalloc": (_c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp,
                                               _c_int, _vp, _vp, _vp]),
 }

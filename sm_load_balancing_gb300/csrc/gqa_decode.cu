@@ -292,6 +292,10 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
                       const Params p) {
   constexpr int NH = D / 64;  // 128-byte halves of a row
   extern __shared__ uint8_t smem_raw[];
+  // with programmatic dependent launch this grid may start before the previous
+  // kernel of the stream (e.g. the device planner) has finished: wait for it
+  // before reading any input
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -838,7 +842,17 @@ int launch_d(const DecodeArgs &a) {
       return SKD_ECUDA;
     attr_set = true;
   }
-  gqa_decode_kernel<D><<<a.n_ctas, (HG + 1) * 32, smem, a.stream>>>(tk, tv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_ctas);
+  cfg.blockDim = dim3((HG + 1) * 32);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gqa_decode_kernel<D>, tk, tv, p) != cudaSuccess) return SKD_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

@@ -42,6 +42,11 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, cuuint32_t rank,
                       const cuuint64_t *gdim, const cuuint64_t *gstride, const cuuint32_t *box,
                       const cuuint32_t *estride, CUtensorMapSwizzle swz);
 
+// Launch the attention kernels with programmatic dependent launch (the kernel
+// may start while the previous kernel of the stream finishes; it waits with
+// griddepcontrol.wait before reading any input). Set by skd_set_pdl.
+bool pdl_enabled();
+
 // Per-CTA timing records enabled by skd_trace_enable (nullptr when off or when
 // the buffer is too small for n_ctas records).
 void *trace_buffer(int n_ctas);

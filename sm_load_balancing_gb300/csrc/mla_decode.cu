@@ -344,6 +344,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tpart, const __grid_constant__ CUtensorMap tout,
                       const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  // with programmatic dependent launch this grid may start before the previous
+  // kernel of the stream (e.g. the device planner) has finished: wait for it
+  // before reading any input
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int worker = blockIdx.x >> 1;
@@ -1106,7 +1110,17 @@ int launch_mla(const DecodeArgs &a) {
       return SKD_ECUDA;
     attr_set = true;
   }
-  mla_decode_kernel<<<2 * a.n_ctas, kThreads, kSmemBytes, a.stream>>>(tmain, trope, tpart, tout, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * a.n_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, tmain, trope, tpart, tout, p) != cudaSuccess) return SKD_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

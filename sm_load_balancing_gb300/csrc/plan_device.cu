@@ -18,15 +18,36 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-__device__ __forceinline__ int64_t bound_of(int64_t c, int64_t total, int64_t n) {
-  return (c * total) / n;
-}
 // CTA owning granule position x (x == total -> last CTA)
 __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
   if (total == 0 || x >= total) return n - 1;
   const int64_t c = ((x + 1) * n + total - 1) / total - 1;
   return c < n - 1 ? c : n - 1;
 }
+
+// Walks bound(c) = floor(c*total/n) for c = c0, c0+1, ... with one division at
+// the start and additions after it (an item can span hundreds of CTAs, and a
+// 64-bit division per step made the planner slow for short batches).
+struct BoundWalk {
+  int64_t lo, hi, q, r, acc, n;  // lo = bound(c), hi = bound(c+1), acc = (c+1)*total mod n
+  __device__ BoundWalk(int64_t c, int64_t total, int64_t n_) : n(n_) {
+    q = total / n;
+    r = total - q * n;
+    lo = (c * total) / n;
+    const int64_t x = (c + 1) * total;
+    hi = x / n;
+    acc = x - hi * n;
+  }
+  __device__ void next() {
+    lo = hi;
+    hi += q;
+    acc += r;
+    if (acc >= n) {
+      acc -= n;
+      ++hi;
+    }
+  }
+};
 
 // In-place exclusive scan of a[0..len) (int32) by the whole block; returns the total.
 __device__ int block_exclusive_scan(int32_t *a, int len, int32_t *warp_sums, int32_t *carry_sm) {
@@ -76,6 +97,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   __shared__ int32_t carry;
   __shared__ int32_t err;
   const int tid = threadIdx.x;
+  // the attention kernel that follows may be scheduled now: it waits for this
+  // grid to complete (griddepcontrol.wait) before reading the plan
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const PlanOffsets off = plan_offsets(batch, ngrp, n);
   const int64_t items = int64_t(batch) * ngrp;
   int32_t *nsplit = plan + off.nsplit;
@@ -128,8 +152,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
       ns = 1;
     } else {
       const int64_t cf = cta_of(s, total, n), cl = cta_of(e - 1, total, n);
-      for (int64_t c = cf; c <= cl; ++c) {
-        if (bound_of(c + 1, total, n) <= bound_of(c, total, n)) continue;  // empty chunk
+      BoundWalk bw(cf, total, n);
+      for (int64_t c = cf; c <= cl; ++c, bw.next()) {
+        if (bw.hi <= bw.lo) continue;  // empty chunk
         atomicAdd(&cnt[c], 1);
         atomicMin(&first[c], int(i));
         ++ns;
@@ -162,8 +187,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     } else {
       const int64_t cf = cta_of(s, total, n), cl = cta_of(e - 1, total, n);
       int k = 0;
-      for (int64_t c = cf; c <= cl; ++c) {
-        const int64_t lo_c = bound_of(c, total, n), hi_c = bound_of(c + 1, total, n);
+      BoundWalk bw(cf, total, n);
+      for (int64_t c = cf; c <= cl; ++c, bw.next()) {
+        const int64_t lo_c = bw.lo, hi_c = bw.hi;
         if (hi_c <= lo_c) continue;
         const int64_t lo = s > lo_c ? s : lo_c, hi = e < hi_c ? e : hi_c;
         const int64_t tb = (lo - s) * kGranule;

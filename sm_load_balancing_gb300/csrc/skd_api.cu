@@ -23,6 +23,7 @@ EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 
 void *g_trace = nullptr;
+bool g_pdl = true;
 size_t g_trace_bytes = 0;
 
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -44,6 +45,8 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, cuuint32_t rank,
   return g_encode(map, dt, rank, gaddr, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
+
+bool pdl_enabled() { return g_pdl; }
 
 void *trace_buffer(int n_ctas) {
   return (g_trace && g_trace_bytes >= size_t(n_ctas) * SKD_TRACE_RECORD_BYTES) ? g_trace : nullptr;
@@ -205,6 +208,11 @@ int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_
   a.lse = lse;
   a.stream = static_cast<cudaStream_t>(stream);
   return shape->kind == SKD_KIND_GQA ? launch_gqa(a) : launch_mla(a);
+}
+
+int skd_set_pdl(int enable) {
+  g_pdl = enable != 0;
+  return SKD_OK;
 }
 
 int skd_trace_enable(void *trace_dev, size_t bytes) {
