@@ -45,7 +45,8 @@ def _args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_gqa")
-    ap.add_argument("--mode", choices=["streamk", "round_robin"], default="streamk")
+    ap.add_argument("--mode", choices=["streamk", "round_robin", "fixed_split"], default="streamk",
+                    help="fixed_split = the two-kernel split-KV comparator (fixed splits + combine kernel)")
     ap.add_argument("--seg-cost", type=int, default=None,
                     help="planner's per-segment cost in granules (default: the library's per-kind default)")
     ap.add_argument("--n-ctas", type=int, default=None)
@@ -307,9 +308,11 @@ def run_ours(a):
     lse = torch.empty(w.batch, w.q_tokens, w.num_q_heads, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    two_kernel = a.mode == "fixed_split"
+
     def step():
         skd.decode_attention(q, k, v, pt, sl, plan_d, ws, scale=w.scale, causal=w.causal, n_ctas=n,
-                             out=out, lse=lse, shape=shape, stream=stream)
+                             out=out, lse=lse, shape=shape, stream=stream, two_kernel=two_kernel)
 
     def barrier():
         if world > 1:
@@ -375,7 +378,7 @@ def run_ours(a):
             sl_d.copy_(sl_h, non_blocking=True)
             plan_dd.copy_(plan_pin, non_blocking=True)
             skd.decode_attention(q_d, k, v, pt_d, sl_d, plan_dd, ws, scale=w.scale, causal=w.causal,
-                                 n_ctas=n, out=out, lse=lse, shape=shape, stream=stream)
+                                 n_ctas=n, out=out, lse=lse, shape=shape, stream=stream, two_kernel=two_kernel)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
             torch.cuda.current_stream().synchronize()

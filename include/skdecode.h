@@ -75,7 +75,10 @@ typedef enum skd_kind { SKD_KIND_GQA = 0, SKD_KIND_MLA = 1 } skd_kind;
 
 typedef enum skd_plan_mode {
   SKD_PLAN_STREAMK = 0,      /* one-wave near-equal split (the method) */
-  SKD_PLAN_ROUND_ROBIN = 1   /* whole (request, kv head) items dealt in turn; comparator */
+  SKD_PLAN_ROUND_ROBIN = 1,  /* whole (request, kv head) items dealt in turn; comparator */
+  SKD_PLAN_FIXED_SPLIT = 2   /* every item cut into the same number of splits, merged by a
+                                separate combine kernel (skd_decode_attention_split_combine);
+                                the two-kernel split-KV comparator */
 } skd_plan_mode;
 
 /* Bits of the device error word (see skd_read_error). */
@@ -157,6 +160,18 @@ int skd_decode_plan_weighted(const int32_t *seqlens_host, int batch, int num_kv_
 int skd_decode_plan_weighted_device(const int32_t *seqlens_dev, int batch, int num_kv_heads, int page_size,
                                     int n_ctas, int seg_cost, void *plan_dev, size_t plan_bytes,
                                     void *stream);
+
+/* The two-kernel split-KV comparator (the design the pages measure MeldKernel
+ * against: split-KV with fixed splits and a separate combine pass). Same
+ * arguments as skd_decode_attention; plan_dev should come from skd_decode_plan
+ * with mode SKD_PLAN_FIXED_SPLIT. The attention kernel writes every split's
+ * partial state (m, l, acc) to the workspace without counting arrivals, then a
+ * second kernel (one CTA per request and kv-head group) merges each item's
+ * splits in split order and writes out / lse. Two launches on `stream`. */
+int skd_decode_attention_split_combine(const skd_shape_t *shape, const void *q, const void *k_pages,
+                                       const void *v_pages, const int32_t *page_table, const int32_t *seqlens,
+                                       const void *plan_dev, int n_ctas, void *ws, size_t ws_bytes, void *out,
+                                       float *lse, void *stream);
 
 /* Launch option (process-wide, default on): launch the attention kernel with
  * programmatic dependent launch, so that it can be scheduled while the

@@ -24,6 +24,10 @@ round_robin_split
     article ("GLM-5.2-FP8 ... B300", MegaRTP KernelPlan paragraph) deals tile
     tasks to worker queues. It is the unbalanced comparator.
 
+fixed_split
+    The two-kernel split-KV comparator: a fixed number of splits per item,
+    merged afterwards by a separate combine step.
+
 round_robin_queues / list_schedule
     The two worked examples the pages print: the MegaRTP queue fill
     (732 tasks over 148 queues) and the 4-SM / 8-task timeline of the Q&A page.
@@ -96,6 +100,32 @@ def round_robin_split(seqlens: Sequence[int], num_kv_heads: int, n_ctas: int) ->
         segments[c].append((i, 0, L[i // num_kv_heads]))
         item_splits.append([(c, 0, L[i // num_kv_heads])])
     return dict(segments=segments, item_splits=item_splits)
+
+
+def fixed_split(seqlens: Sequence[int], num_kv_heads: int, n_ctas: int, granule: int = 16) -> Dict:
+    """The two-kernel comparator's split (FlashDecoding-style split-KV, which
+    the pages measure MeldKernel against): every item is cut into
+    S = max(1, n_ctas // n_items) near-equal granule ranges (fewer if it has
+    fewer granules; one empty range if it has none); the ranges, listed in
+    (item, split) order, are dealt to CTAs in turn."""
+    L = [int(x) for x in seqlens]
+    items = [(b * num_kv_heads + h, L[b]) for b in range(len(L)) for h in range(num_kv_heads)]
+    S = max(1, n_ctas // len(items)) if items else 1
+    flat = []
+    item_splits: List[List[Tuple[int, int]]] = []
+    for i, length in items:
+        g = _ceil_div(length, granule)
+        s = max(1, min(S, g))
+        parts = []
+        for k in range(s):
+            lo, hi = (k * g) // s, ((k + 1) * g) // s
+            parts.append((lo * granule, min(hi * granule, length)))
+        item_splits.append(parts)
+        flat += [(i, tb, te) for tb, te in parts]
+    segments: List[List[Tuple[int, int, int]]] = [[] for _ in range(n_ctas)]
+    for j, seg in enumerate(flat):
+        segments[j % n_ctas].append(seg)
+    return dict(segments=segments, item_splits=item_splits, splits_per_item=S)
 
 
 def round_robin_queues(n_tasks: int, n_queues: int, pad: int = -1) -> np.ndarray:

@@ -26,7 +26,8 @@ __all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention",
            "sm_count", "default_ctas", "default_seg_cost", "make_shape", "set_pdl", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
            "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT"]
 
-_MODES = {"streamk": N.SKD_PLAN_STREAMK, "round_robin": N.SKD_PLAN_ROUND_ROBIN}
+_MODES = {"streamk": N.SKD_PLAN_STREAMK, "round_robin": N.SKD_PLAN_ROUND_ROBIN,
+          "fixed_split": N.SKD_PLAN_FIXED_SPLIT}
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> Optional[int]:
@@ -146,8 +147,11 @@ def decode_attention(q, k_pages, v_pages, page_table, seqlens, plan_dev, ws, *, 
                      causal: Optional[bool] = None, n_ctas: Optional[int] = None,
                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                      shape: Optional[N.Shape] = None,
-                     stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Enqueue one decode-attention launch; returns (out bf16 [B,T,Hq,Dv], lse fp32 [B,T,Hq])."""
+                     stream: Optional[torch.cuda.Stream] = None,
+                     two_kernel: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Enqueue one decode-attention launch; returns (out bf16 [B,T,Hq,Dv], lse fp32 [B,T,Hq]).
+    ``two_kernel``: the split-KV comparator (splits write partial states, a
+    second kernel merges them); meant for plans of mode "fixed_split"."""
     _chk(q, "q", torch.bfloat16)
     _chk(k_pages, "k_pages", torch.bfloat16)
     if v_pages is not None:
@@ -166,7 +170,8 @@ def decode_attention(q, k_pages, v_pages, page_table, seqlens, plan_dev, ws, *, 
         lse = torch.empty(B, T, Hq, dtype=torch.float32, device=q.device)
     n = int(plan_dev[3].item()) if n_ctas is None else int(n_ctas)
     vp = k_pages if v_pages is None else v_pages
-    N.check("skd_decode_attention", N.lib().skd_decode_attention(
+    fn = "skd_decode_attention_split_combine" if two_kernel else "skd_decode_attention"
+    N.check(fn, getattr(N.lib(), fn)(
         ctypes.byref(shape), q.data_ptr(), k_pages.data_ptr(), vp.data_ptr(), page_table.data_ptr(),
         seqlens.data_ptr(), plan_dev.data_ptr(), n, ws.data_ptr(), ws.numel(), out.data_ptr(),
         lse.data_ptr(), _stream_ptr(stream)))

@@ -65,6 +65,7 @@ struct Params {
   float scale_log2;
   int64_t slot_floats, head_floats;
   long long *trace;
+  int defer;  // 1: splits write their partial states and a combine kernel merges them
 };
 
 // Merge `n` partial states of head h (slots base, base+stride, ...) in slot
@@ -689,7 +690,7 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
         }
       }
     }
-    if (split) {
+    if (split && !p.defer) {
       // Publish the partial and count arrivals; the last split merges. The
       // barrier orders every consumer thread's partial writes before thread
       // 0's release-acquire atomic, which publishes them GPU-wide.
@@ -763,6 +764,51 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
   }
 }
 
+// The comparator's second kernel: one CTA per work item, warp h merges head h
+// of the item's splits (all of them, in split order) and writes out / lse.
+template <int D>
+__global__ void __launch_bounds__(kMaxHG * 32, 1) gqa_combine_kernel(const Params p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int item = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const PlanOffsets off = plan_offsets(p.batch, p.NG, p.plan[PH_NCTAS]);
+  const int nsp = p.plan[off.nsplit + item], s0 = p.plan[off.slot0 + item];
+  if (nsp < 2 || h >= p.HG) return;
+  const int b = item / p.NG, head = (item - b * p.NG) * p.HG + h;
+  merge_head<D>(p, h, s0, nsp, 1, true, b, head, lane);
+}
+
+template <int D>
+int launch_combine_d(const DecodeArgs &a) {
+  const skd_shape_t &s = a.shape;
+  const int HG = head_group(s.num_kv_heads);
+  Params p = {};
+  p.plan = a.plan;
+  uint8_t *ws = static_cast<uint8_t *>(a.ws);
+  p.partials = reinterpret_cast<float *>(ws + a.wl.partials);
+  p.out = static_cast<__nv_bfloat16 *>(a.out);
+  p.lse = a.lse;
+  p.batch = s.batch;
+  p.T = s.q_tokens;
+  p.Hq = s.num_q_heads;
+  p.HG = HG;
+  p.NG = s.num_kv_heads / HG;
+  p.G = s.num_q_heads / s.num_kv_heads;
+  p.rows = p.G * s.q_tokens;
+  p.slot_floats = a.wl.slot_floats;
+  p.head_floats = a.wl.head_floats;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.batch * p.NG);
+  cfg.blockDim = dim3(HG * 32);
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gqa_combine_kernel<D>, p) != cudaSuccess) return SKD_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
+}
+
 template <int D>
 int launch_d(const DecodeArgs &a) {
   constexpr int NH = D / 64;
@@ -816,6 +862,7 @@ int launch_d(const DecodeArgs &a) {
   p.slot_floats = a.wl.slot_floats;
   p.head_floats = a.wl.head_floats;
   p.trace = static_cast<long long *>(trace_buffer(a.n_ctas));
+  p.defer = a.defer_merge ? 1 : 0;
 
   // shared memory: stages | Q slots | zero row | barriers | flags
   p.tile_bytes = HG * NH * kGranule * 128;
@@ -857,6 +904,13 @@ int launch_d(const DecodeArgs &a) {
 }
 
 }  // namespace
+
+int launch_gqa_combine(const DecodeArgs &a) {
+  if (a.shape.batch == 0) return SKD_OK;
+  if (a.shape.head_dim_qk == 128) return launch_combine_d<128>(a);
+  if (a.shape.head_dim_qk == 64) return launch_combine_d<64>(a);
+  return SKD_EUNSUPPORTED;
+}
 
 int launch_gqa(const DecodeArgs &a) {
   const int D = a.shape.head_dim_qk;

@@ -30,10 +30,14 @@ struct DecodeArgs {
   void *out;
   float *lse;
   cudaStream_t stream;
+  bool defer_merge = false;  // splits only write their partial states (two-kernel comparator)
 };
 
 int launch_gqa(const DecodeArgs &a);
 int launch_mla(const DecodeArgs &a);
+// the comparator's second kernel: merge every split item's partial states
+int launch_gqa_combine(const DecodeArgs &a);
+int launch_mla_combine(const DecodeArgs &a);
 int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n_ctas, int seg_cost, int32_t *plan,
                        cudaStream_t stream);
 

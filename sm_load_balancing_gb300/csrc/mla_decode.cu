@@ -110,6 +110,7 @@ struct Params {
   float scale_log2;
   int64_t slot_floats;
   long long *trace;
+  int defer;  // 1: splits write their partial states and a combine kernel merges them
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -793,7 +794,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nsp = plan[off.nsplit + b], s0 = plan[off.slot0 + b];
         ptx::named_bar(1, 256);  // previous use of the decision word is over
         if (threadIdx.x == 64)
-          *decision = (!*cx.abort && ld_acquire_gpu(p.item_cnt + b) == nsp - 1) ? 1 : 0;
+          *decision = (!p.defer && !*cx.abort && ld_acquire_gpu(p.item_cnt + b) == nsp - 1) ? 1 : 0;
         ptx::named_bar(1, 256);
         // all other splits already published: merge from TMEM without writing this one
         const bool own_tmem = *decision != 0;
@@ -818,7 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::named_bar(1, 256);
           if (threadIdx.x == 64) {
             int lst = 0;
-            if (!*cx.abort) {
+            if (!*cx.abort && !p.defer) {
               __threadfence();
               lst = ptx::atom_add_acq_rel_gpu(p.item_cnt + b, 1) == nsp - 1 ? 1 : 0;
             }
@@ -1103,6 +1104,7 @@ int launch_mla(const DecodeArgs &a) {
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.slot_floats = a.wl.slot_floats;
   p.trace = static_cast<long long *>(trace_buffer(2 * a.n_ctas));
+  p.defer = a.defer_merge ? 1 : 0;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
@@ -1121,6 +1123,71 @@ int launch_mla(const DecodeArgs &a) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, tmain, trope, tpart, tout, p) != cudaSuccess) return SKD_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
+}
+
+// The comparator's second kernel: one CTA per request, thread (row, half)
+// merges one head row's 256 value columns over all splits in split order
+// (partial O is stored transposed, so consecutive rows are consecutive words).
+__global__ void __launch_bounds__(256, 1) mla_combine_kernel(const Params p, int n_workers) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x, row = threadIdx.x & 127, col0 = (threadIdx.x >> 7) * 256;
+  const PlanOffsets off = plan_offsets(p.batch, 1, n_workers);
+  const int nsp = p.plan[off.nsplit + b], s0 = p.plan[off.slot0 + b];
+  if (nsp < 2) return;
+  float Mx = -INFINITY;
+  for (int sp = 0; sp < nsp; ++sp)
+    Mx = fmaxf(Mx, __ldcg(p.partials + int64_t(s0 + sp) * p.slot_floats + kHeads * kDv + row));
+  const float Mu = Mx == -INFINITY ? 0.f : Mx;
+  float lam = 0.f, lamf = 0.f;
+  for (int sp = 0; sp < nsp; ++sp) {
+    const float *ps = p.partials + int64_t(s0 + sp) * p.slot_floats + kHeads * kDv;
+    const float f = exp2f(__ldcg(ps + row) - Mu);
+    lam += __ldcg(ps + kHeads + row) * f;
+    lamf += __ldcg(ps + 2 * kHeads + row) * f;
+  }
+  const float inv = 1.f / lam;
+  const int64_t orow = int64_t(b) * kHeads + row;
+  for (int c = 0; c < 256; c += 32) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    for (int sp = 0; sp < nsp; ++sp) {
+      const float *ps = p.partials + int64_t(s0 + sp) * p.slot_floats;
+      const float f = exp2f(__ldcg(ps + kHeads * kDv + row) - Mu);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] += __ldcg(ps + (col0 + c + i) * kHeads + row) * f;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) pk[i / 2] = ptx::pack_bf16(acc[i] * inv, acc[i + 1] * inv);
+    uint4 *o4 = reinterpret_cast<uint4 *>(p.out + orow * kDv + col0 + c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
+  if (col0 == 0) p.lse[orow] = (Mx + log2f(lamf)) * kLn2;
+}
+
+int launch_mla_combine(const DecodeArgs &a) {
+  if (a.shape.batch == 0) return SKD_OK;
+  Params p = {};
+  p.plan = a.plan;
+  uint8_t *ws = static_cast<uint8_t *>(a.ws);
+  p.partials = reinterpret_cast<float *>(ws + a.wl.partials);
+  p.out = static_cast<__nv_bfloat16 *>(a.out);
+  p.lse = a.lse;
+  p.batch = a.shape.batch;
+  p.slot_floats = a.wl.slot_floats;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.shape.batch);
+  cfg.blockDim = dim3(256);
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mla_combine_kernel, p, a.n_ctas) != cudaSuccess) return SKD_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

@@ -32,7 +32,7 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
   if (!seqlens && batch > 0) return SKD_EINVAL;
   if (!plan_out || batch < 0 || ngrp <= 0 || n <= 0) return SKD_EINVAL;
   if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
-  if (mode != SKD_PLAN_STREAMK && mode != SKD_PLAN_ROUND_ROBIN) return SKD_EINVAL;
+  if (mode != SKD_PLAN_STREAMK && mode != SKD_PLAN_ROUND_ROBIN && mode != SKD_PLAN_FIXED_SPLIT) return SKD_EINVAL;
   if (seg_cost < 0 || seg_cost > kMaxSegCost || (seg_cost > 0 && mode != SKD_PLAN_STREAMK)) return SKD_EINVAL;
   const PlanOffsets off = plan_offsets(batch, ngrp, n);
   if (plan_bytes < size_t(off.words) * 4) return SKD_EPLAN;
@@ -105,6 +105,39 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
     }
     close_ctas_up_to(n);
     cta_off[n] = int32_t(nseg);
+  } else if (mode == SKD_PLAN_FIXED_SPLIT) {
+    // the two-kernel comparator: every item cut into S = max(1, floor(n /
+    // items)) near-equal granule ranges (fewer if it has fewer granules), so
+    // that all splits fill about one wave; split j of the whole list goes to
+    // CTA j mod n, like a grid of (item, split) blocks
+    const int64_t S = items > 0 ? (n / items > 1 ? n / items : 1) : 1;
+    std::vector<int32_t> all;  // (item, tb, te, slot) in item / split order
+    int64_t slots = 0;
+    for (int64_t i = 0; i < items; ++i) {
+      const int64_t L = seqlens[i / ngrp];
+      const int64_t g = ceil_div(L, kGranule);
+      const int64_t s = g < S ? (g > 0 ? g : 1) : S;
+      nsplit[i] = int32_t(s);
+      slot0[i] = s > 1 ? int32_t(slots) : -1;
+      for (int64_t k = 0; k < s; ++k) {
+        const int64_t lo = (k * g) / s, hi = ((k + 1) * g) / s;
+        all.push_back(int32_t(i));
+        all.push_back(int32_t(lo * kGranule));
+        all.push_back(int32_t(hi * kGranule < L ? hi * kGranule : L));
+        all.push_back(s > 1 ? int32_t(slots + k) : -1);
+      }
+      if (s > 1) slots += s;
+    }
+    const int64_t total_segs = int64_t(all.size()) / 4;
+    if (total_segs > cap) return SKD_EPLAN;
+    for (int64_t c = 0; c < n; ++c) {
+      cta_off[c] = int32_t(nseg);
+      for (int64_t j = c; j < total_segs; j += n) {
+        push(all[4 * j], all[4 * j + 1], all[4 * j + 2]);
+        segs[4 * (nseg - 1) + 3] = all[4 * j + 3];
+      }
+    }
+    cta_off[n] = int32_t(nseg);
   } else {
     // round robin: item i -> CTA i mod n, no splits
     for (int64_t c = 0; c < n; ++c) {
@@ -115,9 +148,12 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
   }
   if (nseg > cap) return SKD_EPLAN;  // cannot happen by construction
 
-  // splits per item (segments of an item are consecutive in the list)
+  // splits per item (segments of an item are consecutive in the list; the
+  // fixed-split mode numbered its slots above)
   int64_t nslots = 0;
-  for (int64_t k = 0; k < nseg;) {
+  if (mode == SKD_PLAN_FIXED_SPLIT)
+    for (int64_t i = 0; i < items; ++i) nslots += nsplit[i] > 1 ? nsplit[i] : 0;
+  for (int64_t k = 0; k < nseg && mode != SKD_PLAN_FIXED_SPLIT;) {
     const int32_t item = segs[4 * k];
     int64_t e = k;
     while (e < nseg && segs[4 * e] == item) ++e;

@@ -178,10 +178,9 @@ int skd_workspace_reset(void *ws, size_t ws_bytes, void *stream) {
   return SKD_OK;
 }
 
-int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_pages,
-                         const void *v_pages, const int32_t *page_table, const int32_t *seqlens,
-                         const void *plan_dev, int n_ctas, void *ws, size_t ws_bytes, void *out,
-                         float *lse, void *stream) {
+static int decode_common(const skd_shape_t *shape, const void *q, const void *k_pages, const void *v_pages,
+                         const int32_t *page_table, const int32_t *seqlens, const void *plan_dev, int n_ctas,
+                         void *ws, size_t ws_bytes, void *out, float *lse, void *stream, bool two_kernel) {
   const int st = validate_shape(shape);
   if (st != SKD_OK) return st;
   if (n_ctas < 1) return SKD_EINVAL;
@@ -207,7 +206,27 @@ int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_
   a.out = out;
   a.lse = lse;
   a.stream = static_cast<cudaStream_t>(stream);
-  return shape->kind == SKD_KIND_GQA ? launch_gqa(a) : launch_mla(a);
+  a.defer_merge = two_kernel;
+  const bool gqa = shape->kind == SKD_KIND_GQA;
+  int st2 = gqa ? launch_gqa(a) : launch_mla(a);
+  if (st2 == SKD_OK && two_kernel) st2 = gqa ? launch_gqa_combine(a) : launch_mla_combine(a);
+  return st2;
+}
+
+int skd_decode_attention(const skd_shape_t *shape, const void *q, const void *k_pages,
+                         const void *v_pages, const int32_t *page_table, const int32_t *seqlens,
+                         const void *plan_dev, int n_ctas, void *ws, size_t ws_bytes, void *out,
+                         float *lse, void *stream) {
+  return decode_common(shape, q, k_pages, v_pages, page_table, seqlens, plan_dev, n_ctas, ws, ws_bytes, out,
+                       lse, stream, false);
+}
+
+int skd_decode_attention_split_combine(const skd_shape_t *shape, const void *q, const void *k_pages,
+                                       const void *v_pages, const int32_t *page_table, const int32_t *seqlens,
+                                       const void *plan_dev, int n_ctas, void *ws, size_t ws_bytes, void *out,
+                                       float *lse, void *stream) {
+  return decode_common(shape, q, k_pages, v_pages, page_table, seqlens, plan_dev, n_ctas, ws, ws_bytes, out,
+                       lse, stream, true);
 }
 
 int skd_set_pdl(int enable) {

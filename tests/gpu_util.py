@@ -28,7 +28,8 @@ class Dev:
         self.sl = torch.from_numpy(w.seqlens).cuda()
         self.shape = skd.make_shape(self.q, self.k, self.v, self.pt, scale=w.scale, causal=w.causal)
 
-    def run(self, n_ctas=None, mode="streamk", plan=None, ws=None, out=None, lse=None, seg_cost=None):
+    def run(self, n_ctas=None, mode="streamk", plan=None, ws=None, out=None, lse=None, seg_cost=None,
+            two_kernel=False):
         skd = self.skd
         n = skd.default_ctas(self.shape) if n_ctas is None else n_ctas
         if plan is None:
@@ -40,7 +41,7 @@ class Dev:
             ws = skd.workspace(self.shape, n)
         o, l = skd.decode_attention(self.q, self.k, self.v, self.pt, self.sl, plan, ws,
                                     scale=self.w.scale, causal=self.w.causal, n_ctas=n,
-                                    shape=self.shape, out=out, lse=lse)
+                                    shape=self.shape, out=out, lse=lse, two_kernel=two_kernel)
         torch.cuda.synchronize()
         err = skd.read_error(ws)
         return o, l, err, ws

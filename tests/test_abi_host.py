@@ -175,6 +175,34 @@ def test_round_robin_mode_matches_definition(N):
     assert p["nslots"] == 0 and all(ns == 1 for ns in p["nsplit"])
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_fixed_split_mode_matches_definition(N, seed):
+    rng = np.random.default_rng(300 + seed)
+    B = int(rng.integers(1, 40))
+    hkv = int(rng.choice([1, 8, 16]))
+    n = int(rng.choice([1, 7, 76, 152]))
+    seqlens = [int(x) for x in rng.integers(0, 5000, size=B)]
+    if seed % 3 == 0:
+        seqlens[0] = 0
+    st, buf = _host_plan(N, seqlens, hkv, n, mode=2)
+    assert st == 0
+    p = PD.decode(buf)
+    ref = S.fixed_split(seqlens, head_groups(hkv), n)
+    assert [[s_[:3] for s_ in segs] for segs in p["segments"]] == ref["segments"]
+    # splits of an item own consecutive slots in split order, numbered in item order
+    nxt = 0
+    for i, parts in enumerate(ref["item_splits"]):
+        assert p["nsplit"][i] == len(parts)
+        if len(parts) > 1:
+            assert p["slot0"][i] == nxt
+            got = sorted((tb, slot) for segs in p["segments"] for it, tb, te, slot in segs if it == i)
+            assert [slot for _, slot in got] == list(range(nxt, nxt + len(parts)))
+            nxt += len(parts)
+        else:
+            assert p["slot0"][i] == -1
+    assert p["nslots"] == nxt <= 2 * n
+
+
 def test_planner_errors(N):
     st, _ = _host_plan(N, [10, -1], 1, 4)
     assert st == N.SKD_EINVAL

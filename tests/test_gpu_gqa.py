@@ -57,6 +57,21 @@ def test_round_robin_plan_gives_same_result(case):
     _check(w, mode="round_robin")
 
 
+@pytest.mark.parametrize("case", range(len(MEDIUM)))
+@pytest.mark.parametrize("n_ctas", [7, None])
+def test_two_kernel_comparator_fixed_split(case, n_ctas):
+    # fixed splits merged by the separate combine kernel ...
+    w = W.make_custom(seed=case, **MEDIUM[case])
+    _check(w, mode="fixed_split", n_ctas=n_ctas, two_kernel=True)
+
+
+@pytest.mark.parametrize("case", [0, 2, 3])
+def test_fixed_split_plan_with_just_in_time_merge(case):
+    # ... and the same plan merged just in time by the one-kernel entry point
+    w = W.make_custom(seed=case, **MEDIUM[case])
+    _check(w, mode="fixed_split")
+
+
 def test_result_independent_of_plan_and_repeatable():
     w = W.make_custom(seed=11, **MEDIUM[0])
     d = Dev(w)

@@ -29,6 +29,13 @@ def test_mla_ragged_lengths(n_workers):
     _check(_mla([1, 63, 64, 65, 200, 0, 1000, 3000], seed=1), n_ctas=n_workers)
 
 
+@pytest.mark.parametrize("n_workers", [5, None])
+def test_mla_two_kernel_comparator(n_workers):
+    # fixed splits written by every worker, merged by the separate combine kernel
+    _check(_mla([1, 63, 64, 65, 200, 0, 1000, 3000], seed=1), n_ctas=n_workers, mode="fixed_split",
+           two_kernel=True)
+
+
 def test_mla_single_long_request_many_splits():
     _check(_mla([20000], seed=2))
 
