@@ -48,6 +48,7 @@ constexpr int kNst = 3;        // KV ring stages
 constexpr float kTau = 8.f;    // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kTraceWords = SKD_TRACE_RECORD_BYTES / 8;
+constexpr int kEpiBar = 6;  // named barrier of the 8 epilogue warps of rank 0
 
 // shared memory (offsets are the same in both ranks: TMA multicast and DSMEM
 // stores address the partner's buffers by the local offset)
@@ -86,7 +87,7 @@ enum {
   B_Q0,                 // both: the first segment's Q is in TMEM (4 arrivals from rank 0, once)
   B_SF0, B_SF1,         // rank 0: score tiles complete (3 issuers; B_SF1 unused)
   B_SE0, B_SE1,         // rank 0: score tiles read out (8 epilogue warps; B_SE1 unused)
-  B_PF0, B_PF1,         // rank 1: P, factors and flags of the block landed (4 bulk copies)
+  B_PF0, B_PF1,         // rank 1: P, factors and flags of the block landed (2 bulk copies)
   B_PVD0, B_PVD1,       // both: PV of the block that used P buffer 0/1 complete
   B_OR0, B_OR1,         // rank 1: O rescaled / V tail zeroed, PV may run (4)
   B_STF,                // rank 1: segment statistics landed (4 remote)
@@ -390,8 +391,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(cx.bar(B_SF1), 1);
     ptx::mbar_init(cx.bar(B_SE0), 8);
     ptx::mbar_init(cx.bar(B_SE1), 8);
-    ptx::mbar_init(cx.bar(B_PF0), 4);
-    ptx::mbar_init(cx.bar(B_PF1), 4);
+    ptx::mbar_init(cx.bar(B_PF0), 1);
+    ptx::mbar_init(cx.bar(B_PF1), 1);
     ptx::mbar_init(cx.bar(B_PVD0), 1);
     ptx::mbar_init(cx.bar(B_PVD1), 1);
     ptx::mbar_init(cx.bar(B_OR0), 8);
@@ -625,9 +626,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         // the staging tile is free once the previous block's copies have read it
-        if (hc == 0 && lane == 0) bulk_wait_read0();
+        if (warp == 2 && lane == 0) bulk_wait_read0();
         xm[hc * kHeads + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        ptx::named_bar(pair_bar, 64);
+        ptx::named_bar(kEpiBar, 256);  // maxima exchanged; the staging tile is free for every warp
         // scores are scaled into log2 units on the fly: the scale is positive,
         // so the maximum of the scaled scores is the scaled maximum
         const float mx = fmaxf(xm[row], xm[kHeads + row]) * p.scale_log2;
@@ -671,15 +672,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         ptx::fence_proxy_async_smem();  // staged bytes are read by the bulk copy (async proxy)
-        ptx::named_bar(pair_bar, 64);
-        // one bulk copy of the tile into P buffer pb of rank 1 once PV(g-2), its previous reader, is done
-        if (hc == 0 && lane == 0) {
+        ptx::named_bar(kEpiBar, 256);
+        // one bulk copy of the whole 16 KB tile (and one of the four quarters'
+        // factors) into P buffer pb of rank 1 once PV(g-2), its previous
+        // reader, is done: a few large copies keep the hand-over short
+        if (warp == 2 && lane == 0) {
           ok = ok && cx.wait(B_PVD0 + pb, uint32_t(((g >> 1) & 1) ^ 1));
           const uint32_t pf = cx.peer_addr(cx.bar(B_PF0 + pb));
-          arrive_expect_tx_remote_relaxed(pf, kQuarterP + kFaBytes);
-          bulk_s2s(cx.peer_addr(cx.sbase + kOffP + uint32_t(pb) * kPBytes + uint32_t(q4) * kQuarterP), stage,
-                   kQuarterP, pf);
-          bulk_s2s(cx.peer_addr(cx.sbase + kOffFa + uint32_t(pb * 4 + q4) * kFaBytes), fstage, kFaBytes, pf);
+          arrive_expect_tx_remote_relaxed(pf, 4 * (kQuarterP + kFaBytes));
+          bulk_s2s(cx.peer_addr(cx.sbase + kOffP + uint32_t(pb) * kPBytes), cx.sbase + kOffStage, 4 * kQuarterP, pf);
+          bulk_s2s(cx.peer_addr(cx.sbase + kOffFa + uint32_t(pb * 4) * kFaBytes), cx.sbase + kOffFa, 4 * kFaBytes,
+                   pf);
           bulk_commit();
         }
       }
@@ -703,7 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++stn;
       ptx::named_bar(pair_bar, 64);  // xm is free for the next segment
     }
-    if (hc == 0 && lane == 0) bulk_wait_read0();
+    if (warp == 2 && lane == 0) bulk_wait_read0();
     (void)ok;
   } else if (rank == 1 && warp >= 2 && warp < 10) {
     // ================= rank 1 epilogue: O rescale, tails, output ================
