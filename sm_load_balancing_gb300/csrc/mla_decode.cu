@@ -13,14 +13,18 @@
 // One worker = a 2-CTA cluster with a producer/consumer split of the math.
 // TMEM holds 128 lanes x 512 fp32 columns per SM, and the 128x512 fp32 output
 // accumulator alone fills it, so the two contractions live on different SMs:
-//   rank 0 (scores): Q [128 heads][576] sits in its TMEM as the A operand
-//     (loaded once per segment), S = Q K^T runs with M=128 heads, N=64 tokens,
-//     K=576 per 64-token block into a double-buffered TMEM score tile, and its
-//     epilogue warps run the online softmax (one thread per head row) and
-//     write the bf16 probabilities P straight into rank 1's shared memory;
+//   rank 0 (scores): Q [128 heads][576] sits in its TMEM as the A operand. It
+//     arrives once per segment by TMA through the KV ring (three fills ahead of
+//     the segment's blocks) and each of three issuing warps copies the chunks
+//     it uses into TMEM with tcgen05.cp. S = Q K^T runs with M=128 heads, N=64
+//     tokens per 64-token block: each issuer accumulates a third of K=576 into
+//     its own partial tile and the eight epilogue warps add the three, run the
+//     online softmax (two warps per head quarter, one thread per head row and
+//     column half) and stage the bf16 probabilities P, which leave for rank 1
+//     as one 16 KB bulk copy per block;
 //   rank 1 (values): O += P V with M=128, N=2x256, K=64 into its TMEM.
-// Each 64-token block is read from HBM once: one TMA box with the 512 value
-// columns is multicast into both CTAs, the 64 rope columns go to rank 0 only.
+// Each rank streams the block into its own ring: rank 0 reads it from HBM,
+// rank 1 a few microseconds later, mostly from L2, as its last reader.
 // The running maximum is kept per row and only moved (with an O rescale on
 // rank 1) when a block's maximum exceeds it by more than 2^8, so p <= 256 and
 // rescales are rare; l and O stay consistent with the same reference maximum.
@@ -56,6 +60,7 @@ constexpr uint32_t kChunkBytes = kBlk * 128;       // 64 columns x 64 tokens, bf
 constexpr uint32_t kMainBytes = 8 * kChunkBytes;   // value columns [0, 512) of one block
 constexpr uint32_t kPBytes = kHeads * kBlk * 2;    // P of one block: 128 rows x 128 B
 constexpr uint32_t kQuarterP = kPBytes / 4;        // the 32 rows of one epilogue warp
+constexpr uint32_t kQChunkBytes = kHeads * 128;    // Q columns [64 c, 64 c + 64) of all heads, SW128
 constexpr uint32_t kOffRing = 0;                   // [kNst][64 KB], both ranks
 constexpr uint32_t kOffRope = kNst * kMainBytes;   // rank 0: [2][8 KB] columns [512, 576)
 constexpr uint32_t kOffStage = kOffRope + 2 * kChunkBytes;  // rank 0: P staging [4 warps][4 KB]
@@ -83,8 +88,7 @@ enum {
   B_KVF = 0,            // [kNst] block landed (rank 0: 72 KB, rank 1: 64 KB)
   B_KVE = kNst,         // [kNst] stage free (rank 0: QK done, rank 1: PV done)
   B_RE0 = 2 * kNst,     // [2] rank 0: rope slot free (QK done)
-  B_QF = B_RE0 + 2,     // rank 0: Q of the segment is in TMEM (4 epilogue warps)
-  B_Q0,                 // both: the first segment's Q is in TMEM (4 arrivals from rank 0, once)
+  B_Q0 = B_RE0 + 2,     // rank 1: rank 0 has its first Q (1 remote arrival, once)
   B_SF0, B_SF1,         // rank 0: score tiles complete (3 issuers; B_SF1 unused)
   B_SE0, B_SE1,         // rank 0: score tiles read out (8 epilogue warps; B_SE1 unused)
   B_PF0, B_PF1,         // rank 1: P, factors and flags of the block landed (2 bulk copies)
@@ -98,7 +102,6 @@ enum {
 static_assert(B_COUNT <= kNumBar, "barrier count");
 
 struct Params {
-  const __nv_bfloat16 *q;
   const int32_t *page_table;
   const int32_t *seqlens;
   const int32_t *plan;
@@ -158,9 +161,6 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
-}
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 // 2-D tiled store shared -> global (bulk group)
 __device__ __forceinline__ void tma_store2(const CUtensorMap *m, uint32_t src, int c0, int c1) {
@@ -223,6 +223,11 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
           d_tmem),
       "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
       : "memory");
+}
+// TMEM (128 lanes x 8 columns from taddr) <- 128 rows x 32 bytes of shared
+// memory given by an operand descriptor; ordered before later MMAs of the same thread
+__device__ __forceinline__ void tmem_cp128(uint32_t taddr, uint64_t sd) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sd) : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -295,7 +300,7 @@ __device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap *m, uint32_
 
 // trace words 2..11: cycles spent waiting, per barrier kind (lane 0 of each waiting warp)
 __device__ __forceinline__ int trace_word(int i) {
-  return i < B_KVE ? 2 : i < B_QF ? 3 : i == B_QF ? 4 : i <= B_SF1 ? 5 : i <= B_SE1 ? 6 : i <= B_PF1 ? 7
+  return i < B_KVE ? 2 : i < B_Q0 ? 3 : i == B_Q0 ? 4 : i <= B_SF1 ? 5 : i <= B_SE1 ? 6 : i <= B_PF1 ? 7
        : i <= B_PVD1 ? 8 : i <= B_OR1 ? 9 : i == B_STF ? 10 : 11;
 }
 
@@ -344,7 +349,7 @@ __device__ __forceinline__ int num_blocks(int tb, int te) { return (te + kBlk - 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmain, const __grid_constant__ CUtensorMap trope,
                       const __grid_constant__ CUtensorMap tpart, const __grid_constant__ CUtensorMap tout,
-                      const Params p) {
+                      const __grid_constant__ CUtensorMap tq, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // with programmatic dependent launch this grid may start before the previous
   // kernel of the stream (e.g. the device planner) has finished: wait for it
@@ -385,8 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(cx.bar(B_RE0), 1);
     ptx::mbar_init(cx.bar(B_RE0 + 1), 1);
-    ptx::mbar_init(cx.bar(B_QF), 8);
-    ptx::mbar_init(cx.bar(B_Q0), 4);
+    ptx::mbar_init(cx.bar(B_Q0), 1);
     ptx::mbar_init(cx.bar(B_SF0), kQkIssuers);
     ptx::mbar_init(cx.bar(B_SF1), 1);
     ptx::mbar_init(cx.bar(B_SE0), 8);
@@ -429,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // a rank-0 stage is free again as soon as its score MMAs are done; rank 1
     // reads the block a few microseconds later, from L2, as its last reader.
     const uint64_t pol = rank == 0 ? policy_evict_normal() : ptx::policy_evict_first();
-    int g = 0;
+    int g = 0, m = 0;  // KV blocks, ring fills (on rank 0 Q takes three fills per segment)
     bool ok = true;
     for (int si = seg_lo; si < seg_hi && ok; ++si) {
       const int4 sg = segs[si];
@@ -440,9 +444,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int L = p.seqlens[b];
         if (te > L || L > p.max_pages * p.P) atomicOr(p.err, SKD_DEVERR_SEQLEN);
       }
-      for (int w0 = (tb / kBlk) * kBlk; w0 < te && ok; w0 += kBlk, ++g) {
-        const int s = g % kNst;
-        const uint32_t ph = uint32_t(g / kNst) & 1u;
+      if (rank == 0) {
+        // the segment's Q [128 heads][576] comes through the ring ahead of its
+        // blocks, as fills of chunks 0-3, 4-7 and 8 (16 KB each); the issuers
+        // copy it into TMEM
+        for (int qb = 0; qb < 3 && ok; ++qb, ++m) {
+          const int s = m % kNst;
+          if (lane == 0) {
+            ok = cx.wait(B_KVE + s, (uint32_t(m / kNst) & 1u) ^ 1u);
+            if (ok) {
+              const int nch = qb < 2 ? 4 : 1;
+              ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), uint32_t(nch) * kQChunkBytes);
+              for (int c = 0; c < nch; ++c)
+                tma3(cx.sbase + kOffRing + s * kMainBytes + c * kQChunkBytes, &tq, cx.bar(B_KVF + s), 0,
+                     b * kHeads, 4 * qb + c, pol);
+              misc[3] = uint32_t(m + 1);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+      }
+      for (int w0 = (tb / kBlk) * kBlk; w0 < te && ok; w0 += kBlk, ++g, ++m) {
+        const int s = m % kNst;
+        const uint32_t ph = uint32_t(m / kNst) & 1u;
         if (lane == 0) {
           const int j = w0 / p.P;
           int pg = j < p.max_pages ? __ldg(ptab + j) : -1;
@@ -450,9 +474,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             atomicOr(p.err, SKD_DEVERR_PAGE);
             pg = 0;
           }
-          // after the first block, wait for the first Q to be loaded: its
-          // loads would otherwise queue behind the whole KV ring of every worker
-          ok = (g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
+          // rank 1 loads its second block only once rank 0 has its first Q,
+          // which would otherwise queue behind the whole value ring of every worker
+          ok = (rank == 0 || g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
                (rank == 1 || cx.wait(B_RE0 + (g & 1), uint32_t((g >> 1) & 1) ^ 1u));
           if (ok) {
             const int rowk = pg * p.P + (w0 % p.P);
@@ -460,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma3(cx.sbase + kOffRing + s * kMainBytes, &tmain, cx.bar(B_KVF + s), 0, rowk, 0, pol);
             if (rank == 0)
               tma3(cx.sbase + kOffRope + (g & 1) * kChunkBytes, &trope, cx.bar(B_KVF + s), 0, rowk, 8, pol);
-            misc[3] = uint32_t(g + 1);
+            misc[3] = uint32_t(m + 1);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -469,7 +493,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || (rank == 0 && warp >= 10)) {
     // ============================ MMA issuers ================================
     if (lane == 0) {
-      int g = 0, qn = 0;
+      int g = 0;
       bool ok = true;
       if (rank == 0) {
         // issuer qi accumulates latent chunks [3 qi, 3 qi + 3) into its own
@@ -477,16 +501,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int qi = warp == 1 ? 0 : warp - 9;
         constexpr uint32_t id_qk = idesc(kHeads, kBlk, 0);
         const uint32_t dS = tmem + kTS + 64 * qi;
+        int m = 0;  // ring fills, as counted by the producer
         for (int si = seg_lo; si < seg_hi && ok; ++si) {
           const int4 sg = segs[si];
           if (sg.z <= sg.y) continue;
           const int nb = num_blocks(sg.y, sg.z);
-          ok = cx.wait(B_QF, uint32_t(qn & 1));
-          ++qn;
+          // Q of the segment: this issuer copies the three chunks its MMAs use
+          // from the ring into TMEM, once the score MMAs of the previous block
+          // (the last readers of those columns) are complete
+          if (g > 0) ok = cx.wait(B_SF0, uint32_t((g - 1) & 1));
+          for (int qb = 0; qb < 3 && ok; ++qb) ok = cx.wait(B_KVF + (m + qb) % kNst, uint32_t((m + qb) / kNst) & 1u);
+          if (!ok) break;
           tc_fence_after();
-          for (int j = 0; j < nb && ok; ++j, ++g) {
-            const int s = g % kNst;
-            if (!cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u) || !cx.wait(B_SE0, uint32_t(g & 1) ^ 1u)) {
+          if (g == 0 && qi == 0) arrive_remote(cx.peer_addr(cx.bar(B_Q0)));
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc) {
+            const int c = 3 * qi + cc, f = m + c / 4;  // chunk c sits in fill f
+            const uint32_t src = cx.sbase + kOffRing + uint32_t(f % kNst) * kMainBytes + uint32_t(c % 4) * kQChunkBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tmem_cp128(tmem + kTQ + c * 32 + kk * 8, sdesc(src + kk * 32, 16, 1024));
+          }
+          for (int qb = 0; qb < 3; ++qb) umma_commit(cx.bar(B_KVE + (m + qb) % kNst));
+          m += 3;
+          for (int j = 0; j < nb && ok; ++j, ++g, ++m) {
+            const int s = m % kNst;
+            if (!cx.wait(B_KVF + s, uint32_t(m / kNst) & 1u) || !cx.wait(B_SE0, uint32_t(g & 1) ^ 1u)) {
               ok = false;
               break;
             }
@@ -550,48 +589,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int si = seg_lo; si < seg_hi; ++si) {
       const int4 sg = segs[si];
-      const int b = sg.x, tb = sg.y, te = sg.z;
+      const int tb = sg.y, te = sg.z;
       if (te <= tb) continue;
       const int nb = num_blocks(tb, te);
-      // Q of this head into TMEM, chunks [0, 5) by half 0 and [5, 9) by half
-      // 1, in one round of loads (the previous segment's score MMAs have
-      // completed: this thread saw the score tile of its last block)
-      {
-        const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q) + (int64_t(b) * kHeads + row) * (kDk / 8);
-        const int c0 = hc == 0 ? 0 : 5, nc = hc == 0 ? 5 : 4;
-        uint4 v[40];
-#pragma unroll
-        for (int i = 0; i < 40; ++i)
-          if (i < nc * 8) v[i] = __ldg(qrow + c0 * 8 + i);
-#pragma unroll
-        for (int c = 0; c < 5; ++c)
-          if (c < nc) tmem_st32(tmem + kTQ + lane_off + (c0 + c) * 32, reinterpret_cast<const uint32_t *>(v + c * 8));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(cx.bar(B_QF));
-          if (g == 0 && hc == 0) {
-            ptx::mbar_arrive(cx.bar(B_Q0));
-            arrive_remote(cx.peer_addr(cx.bar(B_Q0)));
-          }
-        }
-      }
-      // the next segment's Q rows of this quarter go to L2 a few blocks before they are needed
-      int q_next = -1;
-      for (int sn = si + 1; sn < seg_hi; ++sn)
-        if (segs[sn].z > segs[sn].y) {
-          q_next = segs[sn].x;
-          break;
-        }
-      const int j_pref = max(0, nb - 8);
       float mref = -INFINITY, l = 0.f, lf = 0.f;  // l, lf: this half's sums
       const uint32_t stage = cx.sbase + kOffStage + uint32_t(q4) * kQuarterP;  // the quarter's P rows
       const uint32_t fstage = cx.sbase + kOffFa + uint32_t(q4) * kFaBytes;    // its factors + flag
       for (int j = 0; j < nb; ++j, ++g) {
         const int w0 = (tb / kBlk) * kBlk + j * kBlk;
         const int pb = g & 1;
-        if (j == j_pref && q_next >= 0 && hc == 0 && lane == 0)
-          prefetch_l2(p.q + (int64_t(q_next) * kHeads + q4 * 32) * kDk, 32 * kDk * 2);
         float s[32];
         ok = ok && cx.wait(B_SF0, uint32_t(g & 1));
         tc_fence_after();
@@ -1061,7 +1067,7 @@ int launch_mla(const DecodeArgs &a) {
   const skd_shape_t &s = a.shape;
   if (s.page_size % kBlk != 0) return SKD_EUNSUPPORTED;  // 64-token blocks must not straddle pages
   // latent cache viewed as {64 columns, rows (page*P + slot), 9 column chunks}
-  CUtensorMap tmain, trope, tpart, tout;
+  CUtensorMap tmain, trope, tpart, tout, tq;
   const cuuint64_t gk[3] = {64, cuuint64_t(s.num_pages) * s.page_size, 9};
   const cuuint64_t sk[2] = {cuuint64_t(s.v_row_stride) * 2, 128};
   const cuuint32_t es[3] = {1, 1, 1};
@@ -1071,6 +1077,15 @@ int launch_mla(const DecodeArgs &a) {
       encode_tiled(&trope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k), gk, sk, brope, es,
                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return SKD_EINVAL;
+  // queries [batch * 128 heads][576] viewed as {64 columns, rows, 9 column chunks}, one chunk per box
+  {
+    const cuuint64_t gq[3] = {64, cuuint64_t(s.batch) * kHeads, 9};
+    const cuuint64_t sq[2] = {cuuint64_t(kDk) * 2, 128};
+    const cuuint32_t bq[3] = {64, kHeads, 1};
+    if (encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.q), gq, sq, bq, es,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return SKD_EINVAL;
+  }
   // partial-state slots (O stored transposed) viewed as {128 rows, 512 columns, slots} fp32, boxes of 32 x 32
   {
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
@@ -1089,7 +1104,6 @@ int launch_mla(const DecodeArgs &a) {
       return SKD_EINVAL;
   }
   Params p;
-  p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.page_table = a.page_table;
   p.seqlens = a.seqlens;
   p.plan = a.plan;
@@ -1125,7 +1139,7 @@ int launch_mla(const DecodeArgs &a) {
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, tmain, trope, tpart, tout, p) != cudaSuccess) return SKD_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, tmain, trope, tpart, tout, tq, p) != cudaSuccess) return SKD_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 
