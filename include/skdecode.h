@@ -113,6 +113,14 @@ const char *skd_status_string(int status);
  * intended grid). */
 int skd_device_sm_count(int device, int *sm_count_out);
 
+/* Workers (n_ctas) for one wave of the decode kernel of `shape` on CUDA device
+ * `device`: GQA: one CTA per SM; absorbed MLA: a worker is a cluster of 2 CTAs
+ * (a score SM and a value SM), so the number of such clusters that fit on the
+ * device at once (at most SMs / 2). Any n_ctas >= 1 is valid for the
+ * decode calls; fewer than this leaves SMs idle, more runs in several waves.
+ * Errors: SKD_EINVAL (null pointer or invalid shape), SKD_ECUDA. */
+int skd_default_workers(const skd_shape_t *shape, int device, int *n_out);
+
 /* ---- planner ----------------------------------------------------------- */
 
 /* Bytes of a plan for `batch` requests, `num_kv_heads` heads, `n_ctas` CTAs.
@@ -251,8 +259,11 @@ int skd_decode_attention_noalloc(const skd_shape_t *shape, const void *q, const 
  * total, 6: segments, 7: pipeline stages, 8: SM id, 9: consumer cycles spent
  * publishing and merging partial states (summed), 10: final merges, 11:
  * merge-tree node merges, 12..15: reserved}. Words 2, 3, 7, 9, 10 and 11 are
- * accumulated with atomics: zero the buffer before each launch. A buffer smaller than
- * n_ctas records disables tracing for that launch. Process-wide setting, not
+ * accumulated with atomics: zero the buffer before each launch. An absorbed-MLA
+ * launch writes 2 records per worker (its cluster ranks: 0 score, 1 value):
+ * {0, 1 as above, 2..11: cycles its warps spent waiting, summed per barrier
+ * kind, 14: segments, 15: SM id}. A buffer smaller than n_ctas records
+ * (2 n_ctas for MLA) disables tracing for that launch. Process-wide setting, not
  * thread-safe; pass NULL to disable. Errors: SKD_EINVAL (misaligned pointer). */
 #define SKD_TRACE_RECORD_BYTES 128
 int skd_trace_enable(void *trace_dev, size_t bytes);

@@ -44,9 +44,14 @@ def sm_count(device: Optional[int] = None) -> int:
 
 def default_ctas(shape: Optional[N.Shape] = None, device: Optional[int] = None) -> int:
     """Stream-K workers for one wave: one per SM for GQA; for absorbed MLA a
-    worker is a 2-CTA cluster, so half the SMs."""
-    n = sm_count(device)
-    return n // 2 if (shape is not None and shape.kind == N.SKD_KIND_MLA) else n
+    worker is a 2-CTA cluster (a score SM and a value SM), so the number of
+    such clusters the device holds at once."""
+    if shape is None or shape.kind != N.SKD_KIND_MLA:
+        return sm_count(device)
+    dev = torch.cuda.current_device() if device is None else int(device)
+    v = ctypes.c_int(0)
+    N.check("skd_default_workers", N.lib().skd_default_workers(ctypes.byref(shape), dev, ctypes.byref(v)))
+    return v.value
 
 
 # Fixed per-segment cost of the absorbed-MLA kernel in granules of KV work:

@@ -35,6 +35,7 @@ SIGNATURES = {
     "skd_abi_version": (_c_int, []),
     "skd_status_string": (ctypes.c_char_p, [_c_int]),
     "skd_device_sm_count": (_c_int, [_c_int, ctypes.POINTER(ctypes.c_int)]),
+    "skd_default_workers": (_c_int, [ctypes.POINTER(Shape), _c_int, ctypes.POINTER(ctypes.c_int)]),
     "skd_plan_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "skd_decode_plan": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size]),
     "skd_decode_plan_device": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),

@@ -35,6 +35,8 @@ struct DecodeArgs {
 
 int launch_gqa(const DecodeArgs &a);
 int launch_mla(const DecodeArgs &a);
+// MLA workers (3-CTA clusters) that can be resident at once on the current device
+int mla_resident_workers(int *n);
 // the comparator's second kernel: merge every split item's partial states
 int launch_gqa_combine(const DecodeArgs &a);
 int launch_mla_combine(const DecodeArgs &a);

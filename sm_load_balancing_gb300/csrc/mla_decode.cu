@@ -1063,6 +1063,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+namespace {
+
+int set_smem_attr() {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
+        cudaSuccess)
+      return SKD_ECUDA;
+    attr_set = true;
+  }
+  return SKD_OK;
+}
+
+}  // namespace
+
+int mla_resident_workers(int *n) {
+  if (set_smem_attr() != SKD_OK) return SKD_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 1024);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int v = 0;
+  if (cudaOccupancyMaxActiveClusters(&v, mla_decode_kernel, &cfg) != cudaSuccess) return SKD_ECUDA;
+  *n = v;
+  return SKD_OK;
+}
+
 int launch_mla(const DecodeArgs &a) {
   const skd_shape_t &s = a.shape;
   if (s.page_size % kBlk != 0) return SKD_EUNSUPPORTED;  // 64-token blocks must not straddle pages
@@ -1122,13 +1149,7 @@ int launch_mla(const DecodeArgs &a) {
   p.slot_floats = a.wl.slot_floats;
   p.trace = static_cast<long long *>(trace_buffer(2 * a.n_ctas));
   p.defer = a.defer_merge ? 1 : 0;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
-        cudaSuccess)
-      return SKD_ECUDA;
-    attr_set = true;
-  }
+  if (set_smem_attr() != SKD_OK) return SKD_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.n_ctas);
   cfg.blockDim = dim3(kThreads);

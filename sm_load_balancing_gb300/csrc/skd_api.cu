@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kernels.h"
@@ -122,6 +123,25 @@ int skd_device_sm_count(int device, int *sm_count_out) {
   if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return SKD_ECUDA;
   *sm_count_out = v;
+  return SKD_OK;
+}
+
+int skd_default_workers(const skd_shape_t *shape, int device, int *n_out) {
+  if (!shape || !n_out) return SKD_EINVAL;
+  const int st = validate_shape(shape);
+  if (st != SKD_OK) return st;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return SKD_ECUDA;
+  if (shape->kind == SKD_KIND_GQA) {
+    *n_out = sms;
+    return SKD_OK;
+  }
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) return SKD_ECUDA;
+  int n = 0;
+  const int r = mla_resident_workers(&n);
+  if (cudaSetDevice(cur) != cudaSuccess || r != SKD_OK) return SKD_ECUDA;
+  *n_out = std::max(1, std::min(n, sms / 2));
   return SKD_OK;
 }
 

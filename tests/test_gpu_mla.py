@@ -36,6 +36,37 @@ def test_mla_two_kernel_comparator(n_workers):
            two_kernel=True)
 
 
+def _ramp_scores(w, step):
+    """Scores rise by `step` (natural-log units) per 64-token block: q's rope
+    columns are all 1 and key t's rope columns all 24 * step * (t // 64) / 64,
+    so q.k / 24 gains step * (t // 64); the value columns are untouched."""
+    q = W.bf16_bits_to_fp32(w.q)
+    q[..., 512:] = 1.0
+    w.q[...] = W.fp32_to_bf16_bits(q)
+    P = w.page_size
+    for b, L in enumerate(w.seqlens):
+        for t0 in range(0, int(L), 64):
+            pg = w.page_table[b, t0 // P]
+            n = min(64, int(L) - t0)
+            val = np.float32(24.0 * step * (t0 // 64) / 64.0)
+            w.k_pages[pg, t0 % P:t0 % P + n, 0, 512:] = W.fp32_to_bf16_bits(np.full((n, 64), val, np.float32))
+
+
+@pytest.mark.parametrize("n_workers", [1, 2, None])
+def test_mla_rising_scores_move_the_reference(n_workers):
+    # about 5.8 log2 units per block against the lazy threshold of 8: the
+    # reference moves every block or two and the value CTA rescales O, across
+    # single-block, odd-length and split segments
+    w = _mla([3000, 64, 700, 1, 130, 2000], seed=6)
+    _ramp_scores(w, 4.0)
+    _check(w, n_ctas=n_workers)
+
+
+def test_mla_many_one_block_requests():
+    # every segment is a single block: Q is loaded for every block
+    _check(_mla([1 + (7 * i) % 64 for i in range(41)], seed=7), n_ctas=3)
+
+
 def test_mla_single_long_request_many_splits():
     _check(_mla([20000], seed=2))
 
