@@ -140,3 +140,101 @@ int oracle_decode_f64(int B, int T, int Hq, int Hkv, int Dk, int Dv, int P, int 
     }
     return err;
 }
+
+/* Sparse (top-k) attention: row (b, t, h) attends to the multiset of cache
+ * positions {topk_idx[b][i] : 0 <= i < topk_len[b]} and to nothing else -- the
+ * plain softmax attention of the definition above restricted to the keys an
+ * indexer selected. The GLM-5.2-FP8 decode article (tahou.com; summary and the
+ * related-work paragraph on TileRT) has the layer continue with TopK and
+ * Sparse FlashMLA, whose ranks gather the sparse KV rows named by the top-2048
+ * indices; the pages give no formula, so this is the plain reading. A position
+ * listed twice counts as two keys; no causal mask is applied (the selection
+ * decides visibility); topk_len[b] == 0 gives out = 0 and lse = -inf. Keys are
+ * summed in list order.
+ *
+ * Extra error codes:
+ *   -5  topk_len[b] outside [0, topk_stride]
+ *   -6  a listed position outside [0, seqlens[b])
+ */
+int oracle_decode_sparse_f64(int B, int T, int Hq, int Hkv, int Dk, int Dv, int P, int max_pages,
+                             int num_pages, double scale, const uint16_t *q, const uint16_t *k_pages,
+                             const uint16_t *v_pages, long long v_row_stride, const int32_t *page_table,
+                             const int32_t *seqlens, const int32_t *topk_idx, int topk_stride,
+                             const int32_t *topk_len, const int64_t *rows, long long n_rows, double *out,
+                             double *lse) {
+    if (B < 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Dk <= 0 || Dv <= 0 || P <= 0 ||
+        max_pages <= 0 || v_row_stride < Dv || topk_stride <= 0)
+        return -1;
+    const int G = Hq / Hkv;
+    const long long total_rows = (long long)B * T * Hq;
+    if (rows == NULL) n_rows = total_rows;
+
+    for (int b = 0; b < B; ++b) {
+        int L = seqlens[b];
+        if (L < 0 || (long long)L > (long long)max_pages * P) return -2;
+        int K = topk_len[b];
+        if (K < 0 || K > topk_stride) return -5;
+        for (int i = 0; i < K; ++i) {
+            int j = topk_idx[(long long)b * topk_stride + i];
+            if (j < 0 || j >= L) return -6;
+            int pg = page_table[(long long)b * max_pages + j / P];
+            if (pg < 0 || pg >= num_pages) return -3;
+        }
+    }
+
+    int err = 0;
+#pragma omp parallel
+    {
+        double *sig = NULL;
+        long long cap = 0;
+#pragma omp for schedule(dynamic, 1)
+        for (long long i = 0; i < n_rows; ++i) {
+            long long r = rows ? rows[i] : i;
+            if (r < 0 || r >= total_rows) {
+#pragma omp atomic write
+                err = -1;
+                continue;
+            }
+            const int h = (int)(r % Hq);
+            const int b = (int)(r / ((long long)Hq * T));
+            const int g = h / G;
+            const long long n = topk_len[b];
+            const int32_t *sel = topk_idx + (long long)b * topk_stride;
+            double *o = out + i * (long long)Dv;
+            for (int d = 0; d < Dv; ++d) o[d] = 0.0;
+            if (n <= 0) {
+                lse[i] = -INFINITY;
+                continue;
+            }
+            if (n > cap) {
+                free(sig);
+                cap = n;
+                sig = (double *)malloc(sizeof(double) * (size_t)cap);
+            }
+            const uint16_t *qr = q + r * (long long)Dk;
+            for (long long x = 0; x < n; ++x) {
+                const int j = sel[x];
+                const int pg = page_table[(long long)b * max_pages + j / P];
+                const uint16_t *kr = k_pages + (((long long)pg * P + j % P) * Hkv + g) * (long long)Dk;
+                double acc = 0.0;
+                for (int d = 0; d < Dk; ++d) acc += bf16_to_f64(qr[d]) * bf16_to_f64(kr[d]);
+                sig[x] = scale * acc;
+            }
+            double mu = -INFINITY;
+            for (long long x = 0; x < n; ++x)
+                if (sig[x] > mu) mu = sig[x];
+            double Z = 0.0;
+            for (long long x = 0; x < n; ++x) Z += exp(sig[x] - mu);
+            for (long long x = 0; x < n; ++x) {
+                const double wgt = exp(sig[x] - mu) / Z;
+                const int j = sel[x];
+                const int pg = page_table[(long long)b * max_pages + j / P];
+                const uint16_t *vr = v_pages + (((long long)pg * P + j % P) * Hkv + g) * v_row_stride;
+                for (int d = 0; d < Dv; ++d) o[d] += wgt * bf16_to_f64(vr[d]);
+            }
+            lse[i] = mu + log(Z);
+        }
+        free(sig);
+    }
+    return err;
+}

@@ -13,6 +13,11 @@ Recipe (fixed order of draws from one numpy PCG64 stream per workload):
 For the absorbed-MLA workload there is one latent cache [NP][P][576]; V is the
 first 512 columns of the same rows (row stride 576), so step 5 is skipped.
 
+A top-k selection (sparse MLA) is drawn afterwards from its own stream
+(PCG64 seeded with [seed, 1]), so the cache draws above do not change: request b
+lists K_b = min(k, L_b) distinct positions of [0, L_b), sampled uniformly, in
+random order (an indexer's top-k comes ordered by score, not by position).
+
 bf16 values are produced by rounding fp32 normals to nearest-even; they are kept
 as uint16 bit patterns so that nothing here depends on a bf16 dtype.
 Page-table entries past a request's last page are -1.
@@ -30,6 +35,7 @@ __all__ = [
     "WORKLOADS",
     "make",
     "make_custom",
+    "select_topk",
     "fp32_to_bf16_bits",
     "bf16_bits_to_fp32",
 ]
@@ -85,6 +91,12 @@ class Workload:
     k_pages: np.ndarray          # uint16 [NP][P][Hkv][Dk]
     v_pages: Optional[np.ndarray]  # uint16 [NP][P][Hkv][Dv]; None for MLA (V aliases k_pages)
     seed: int = 0
+    topk_idx: Optional[np.ndarray] = None  # int32 [B][K]: listed cache positions (sparse attention)
+    topk_len: Optional[np.ndarray] = None  # int32 [B]: entries of row b that are listed
+
+    @property
+    def sparse(self) -> bool:
+        return self.topk_idx is not None
 
     @property
     def num_pages(self) -> int:
@@ -101,6 +113,9 @@ class Workload:
 
     @property
     def kv_tokens(self) -> int:
+        """KV rows the attention reads: all cached tokens, or the listed ones."""
+        if self.sparse:
+            return int(self.topk_len.astype(np.int64).sum())
         return int(self.seqlens.astype(np.int64).sum())
 
     def kv_bytes_per_token(self) -> int:
@@ -109,9 +124,13 @@ class Workload:
         return self.num_kv_heads * (self.head_dim_qk + self.head_dim_v) * 2
 
     def algorithmic_bytes(self) -> int:
-        """KV bytes + q + out (bf16) + lse (fp32) + referenced page-table entries."""
+        """KV bytes + q + out (bf16) + lse (fp32) + referenced page-table entries
+        (sparse: one page-table entry and one index per listed position)."""
         P = self.page_size
-        pages = int(sum((int(L) + P - 1) // P for L in self.seqlens))
+        if self.sparse:
+            pages = 2 * self.kv_tokens
+        else:
+            pages = int(sum((int(L) + P - 1) // P for L in self.seqlens))
         rows = self.batch * self.q_tokens * self.num_q_heads
         return (self.kv_tokens * self.kv_bytes_per_token()
                 + rows * self.head_dim_qk * 2 + rows * self.head_dim_v * 2 + rows * 4 + pages * 4)
@@ -131,7 +150,8 @@ class Workload:
                     num_q_heads=self.num_q_heads, num_kv_heads=self.num_kv_heads,
                     head_dim_qk=self.head_dim_qk, head_dim_v=self.head_dim_v,
                     page_size=self.page_size, causal=self.causal, mla=self.mla,
-                    kv_tokens=self.kv_tokens, seed=self.seed)
+                    kv_tokens=self.kv_tokens, seed=self.seed,
+                    **({"topk": int(self.topk_idx.shape[1])} if self.sparse else {}))
 
 
 def _assemble(name, rng, seqlens, *, T, Hq, Hkv, Dk, Dv, P, causal, scale, mla, seed,
@@ -191,6 +211,25 @@ def _mla(seed):
                      Dv=512, P=64, causal=False, scale=1.0 / math.sqrt(576), mla=True, seed=seed)
 
 
+def select_topk(w: Workload, k: int, seed: Optional[int] = None, name: Optional[str] = None) -> Workload:
+    """The same cache with a top-k selection per request (see the module docstring)."""
+    rng = np.random.Generator(np.random.PCG64([w.seed if seed is None else seed, 1]))
+    B = w.batch
+    idx = np.zeros((B, max(k, 1)), dtype=np.int32)
+    n = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        L = int(w.seqlens[b])
+        kb = min(k, L)
+        if kb > 0:
+            idx[b, :kb] = rng.permutation(rng.choice(L, size=kb, replace=False)).astype(np.int32)
+        n[b] = kb
+    return dataclasses.replace(w, topk_idx=idx, topk_len=n, name=name or w.name + f"_top{k}")
+
+
+def _mla_sparse(seed):
+    return select_topk(_mla(seed), 2048, name="mla_sparse_top2048_b64_h128_d576v512_p64")
+
+
 def _speculative(seed):
     rng = np.random.Generator(np.random.PCG64(seed))
     L = rng.integers(4096, 32768, size=16, endpoint=True)
@@ -205,11 +244,12 @@ WORKLOADS = {
     "skewed_gqa": _skewed,
     "mla_absorbed": _mla,
     "speculative_gqa": _speculative,
+    "mla_sparse_top2048": _mla_sparse,
 }
 
 
 def make(name: str, seed: int = 0) -> Workload:
-    """Build one of the five named workloads (full size)."""
+    """Build one of the named workloads (full size)."""
     return WORKLOADS[name](seed)
 
 
@@ -241,7 +281,7 @@ def draw_seqlens(name: str, seed: int = 0) -> np.ndarray:
         short = rng.integers(64, 1024, size=63, endpoint=True)
         pos = int(rng.integers(0, 64))
         return np.insert(short, pos, 131072).astype(np.int32)
-    if name == "mla_absorbed":
+    if name in ("mla_absorbed", "mla_sparse_top2048"):
         return rng.integers(1024, 16384, size=64, endpoint=True).astype(np.int32)
     if name == "speculative_gqa":
         return rng.integers(4096, 32768, size=16, endpoint=True).astype(np.int32)
