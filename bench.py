@@ -33,6 +33,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention µs/call and achieved HBM TB/s (% of roofline) on 1 GB300"
+L2_BYTES = 129 * 1000 * 1000
+FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SRC = {"gqa": "sm_load_balancing_gb300/csrc/gqa_decode.cu",
               "mla": "sm_load_balancing_gb300/csrc/mla_decode.cu"}
@@ -206,31 +208,33 @@ def _cpu_oracle_sample(w, target_s):
     from oracle import attention as A
     A.build()
     rows_per_req = w.q_tokens * w.num_q_heads
+    decode = A.decode_sparse_workload if w.sparse else A.decode_workload
+    lens = w.topk_len if w.sparse else w.seqlens  # KV rows each request reads
     # probe one request to size the sample
     order = list(range(w.batch))
     t0 = time.perf_counter()
-    A.decode_workload(w, rows=list(range(rows_per_req)))
-    per_req = max(time.perf_counter() - t0, 1e-4) / max(int(w.seqlens[0]), 1)
+    decode(w, rows=list(range(rows_per_req)))
+    per_req = max(time.perf_counter() - t0, 1e-4) / max(int(lens[0]), 1)
     budget_tokens = target_s / per_req
     chosen, toks = [], 0
     for b in order:
-        if chosen and toks + int(w.seqlens[b]) > budget_tokens:
+        if chosen and toks + int(lens[b]) > budget_tokens:
             break
         chosen.append(b)
-        toks += int(w.seqlens[b])
+        toks += int(lens[b])
     rows = [b * rows_per_req + r for b in chosen for r in range(rows_per_req)]
     # repeat a short sample until it has run for a few seconds (stable timing)
     reps, dt = 0, 0.0
     while reps == 0 or (dt < min(3.0, target_s) and reps < 1000):
         t0 = time.perf_counter()
-        A.decode_workload(w, rows=rows)
+        decode(w, rows=rows)
         dt += time.perf_counter() - t0
         reps += 1
     frac = toks / max(w.kv_tokens, 1)
     sample_bytes = w.algorithmic_bytes() * frac * reps
     desc = (f"all {rows_per_req} query rows of requests 0..{chosen[-1]} "
             f"({len(chosen)} of {w.batch} requests, {toks} of {w.kv_tokens} KV tokens), "
-            f"{reps} repetition(s), fp64 C oracle, OpenMP")
+            f"{reps} repetition(s), fp64 C oracle{' (sparse)' if w.sparse else ''}, OpenMP")
     return sample_bytes / dt, A.num_threads(), desc, dt
 
 
@@ -298,10 +302,17 @@ def run_ours(a):
     v = None if w.mla else bf16(w.v_pages).to(dev)
     pt = torch.from_numpy(w.page_table).to(dev)
     sl = torch.from_numpy(w.seqlens).to(dev)
+    sparse = w.sparse
+    if sparse:
+        if a.mode == "fixed_split":
+            raise SystemExit("the two-kernel comparator is not built for the sparse path")
+        ti = torch.from_numpy(w.topk_idx).to(dev)
+        tl = torch.from_numpy(w.topk_len).to(dev)
+    plan_lens = w.topk_len if sparse else w.seqlens  # the planner splits what each request reads
     shape = skd.make_shape(q, k, v, pt, scale=w.scale, causal=w.causal)
     n = a.n_ctas or skd.default_ctas(shape)
     seg_cost = 0 if a.mode != "streamk" else (skd.default_seg_cost(shape) if a.seg_cost is None else a.seg_cost)
-    plan_h = skd.plan(w.seqlens, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)
+    plan_h = skd.plan(plan_lens, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)
     plan_d = plan_h.to(dev)
     ws = skd.workspace(shape, n, dev)
     out = torch.empty(w.batch, w.q_tokens, w.num_q_heads, w.head_dim_v, dtype=torch.bfloat16, device=dev)
@@ -311,8 +322,19 @@ def run_ours(a):
     two_kernel = a.mode == "fixed_split"
 
     def step():
-        skd.decode_attention(q, k, v, pt, sl, plan_d, ws, scale=w.scale, causal=w.causal, n_ctas=n,
-                             out=out, lse=lse, shape=shape, stream=stream, two_kernel=two_kernel)
+        if sparse:
+            skd.decode_attention_sparse(q, k, pt, sl, ti, tl, plan_d, ws, scale=w.scale, n_ctas=n, out=out,
+                                        lse=lse, shape=shape, stream=stream)
+        else:
+            skd.decode_attention(q, k, v, pt, sl, plan_d, ws, scale=w.scale, causal=w.causal, n_ctas=n,
+                                 out=out, lse=lse, shape=shape, stream=stream, two_kernel=two_kernel)
+
+    # bytes a step reads: when they are under twice L2 (129 MB), part of them could
+    # still be in L2 from the previous step, so a 256 MB write evicts it before
+    # every timed step (outside the per-step events)
+    flush = None
+    if w.algorithmic_bytes() < 2 * L2_BYTES:
+        flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def barrier():
         if world > 1:
@@ -333,6 +355,8 @@ def run_ours(a):
     t_all1 = torch.cuda.Event(enable_timing=True)
     t_all0.record(stream)
     for i in range(a.steps):
+        if flush is not None:
+            flush.zero_()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -350,12 +374,13 @@ def run_ours(a):
 
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
+        t = torch.tensor([total_ms, mean_kernel_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms, mean_kernel_ms = float(t[0].item()), float(t[1].item())
 
     alg_bytes = w.algorithmic_bytes()
-    ms_per_step = total_ms / a.steps
+    # with flushes in the loop a step is its own event span, else the whole loop / steps
+    ms_per_step = (mean_kernel_ms if flush is not None else total_ms / a.steps)
     value = world * alg_bytes / (ms_per_step * 1e-3) / 1e12  # TB/s, all ranks
 
     # ---- e2e through the public API with host buffers ----
@@ -369,16 +394,27 @@ def run_ours(a):
         q_d, pt_d, sl_d = torch.empty_like(q), torch.empty_like(pt), torch.empty_like(sl)
         plan_pin = torch.empty_like(plan_h).pin_memory()
         plan_dd = torch.empty_like(plan_d)
+        if sparse:
+            ti_h = torch.from_numpy(w.topk_idx).pin_memory()
+            tl_h = torch.from_numpy(w.topk_len).pin_memory()
+            ti_d, tl_d = torch.empty_like(ti), torch.empty_like(tl)
 
         def e2e_step():
-            p = skd.plan(sl_h, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)  # host planner
+            lens_h = tl_h if sparse else sl_h
+            p = skd.plan(lens_h, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)  # host planner
             plan_pin.copy_(p)
             q_d.copy_(q_h, non_blocking=True)
             pt_d.copy_(pt_h, non_blocking=True)
             sl_d.copy_(sl_h, non_blocking=True)
             plan_dd.copy_(plan_pin, non_blocking=True)
-            skd.decode_attention(q_d, k, v, pt_d, sl_d, plan_dd, ws, scale=w.scale, causal=w.causal,
-                                 n_ctas=n, out=out, lse=lse, shape=shape, stream=stream, two_kernel=two_kernel)
+            if sparse:
+                ti_d.copy_(ti_h, non_blocking=True)
+                tl_d.copy_(tl_h, non_blocking=True)
+                skd.decode_attention_sparse(q_d, k, pt_d, sl_d, ti_d, tl_d, plan_dd, ws, scale=w.scale, n_ctas=n,
+                                            out=out, lse=lse, shape=shape, stream=stream)
+            else:
+                skd.decode_attention(q_d, k, v, pt_d, sl_d, plan_dd, ws, scale=w.scale, causal=w.causal,
+                                     n_ctas=n, out=out, lse=lse, shape=shape, stream=stream, two_kernel=two_kernel)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
             torch.cuda.current_stream().synchronize()
@@ -398,11 +434,14 @@ def run_ours(a):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             t_e2e = float(t.item())
         h2d = q_h.numel() * 2 + pt_h.numel() * 4 + sl_h.numel() * 4 + plan_pin.numel() * 4
+        if sparse:
+            h2d += ti_h.numel() * 4 + tl_h.numel() * 4
         d2h = out_h.numel() * 2 + lse_h.numel() * 4
         e2e = {"value": world * alg_bytes / t_e2e / 1e12, "unit": "TB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "us_per_step": t_e2e * 1e6, "steps": n_e2e,
-               "note": "host planner + pinned H2D of q/seqlens/page table/plan + kernel + D2H of out/lse; KV cache resident"}
+               "note": "host planner + pinned H2D of q/seqlens/page table/plan" + ("/top-k lists" if sparse else "")
+                       + " + kernel + D2H of out/lse; KV cache resident"}
         if skd.read_error(ws) != 0:
             raise RuntimeError("device error in e2e loop")
 
@@ -416,14 +455,15 @@ def run_ours(a):
         "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
         "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
                    "n_ctas": n, "plan": a.mode, "seg_cost": seg_cost, "algorithmic_bytes": alg_bytes,
-                   "l2": "no flush: KV per step is larger than L2 (129 MB)",
+                   "l2": ("flushed before each timed step (256 MB write, outside the step's events)"
+                          if flush is not None else "no flush: KV per step is larger than L2 (129 MB)"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": f"{kind}_decode_kernel", "launch_ms_mean": mean_kernel_ms,
                      "launch_ms_median": statistics.median(per)},
         "e2e": e2e,
-        "gpu_launches": a.steps,
+        "gpu_launches": a.steps * (2 if two_kernel else 1),
         "clocks": ck,
     }
     if launch is not None:

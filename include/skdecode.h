@@ -86,6 +86,7 @@ typedef enum skd_plan_mode {
 #define SKD_DEVERR_SEQLEN 0x2    /* a seqlen disagrees with the plan or the page table size */
 #define SKD_DEVERR_PAGE 0x4      /* a page id outside [0, num_pages) */
 #define SKD_DEVERR_TIMEOUT 0x8   /* a bounded wait inside the kernel gave up */
+#define SKD_DEVERR_INDEX 0x10    /* sparse: a listed position outside [0, seqlens[b]) */
 
 typedef struct skd_shape {
   int32_t batch;             /* B >= 0 */
@@ -180,6 +181,25 @@ int skd_decode_attention_split_combine(const skd_shape_t *shape, const void *q, 
                                        const void *v_pages, const int32_t *page_table, const int32_t *seqlens,
                                        const void *plan_dev, int n_ctas, void *ws, size_t ws_bytes, void *out,
                                        float *lse, void *stream);
+
+/* Sparse (top-k) absorbed-MLA decode attention: request b attends only to
+ * the cache positions topk_idx[b * topk_stride + i], i < topk_len[b] (device
+ * int32 arrays; positions in [0, seqlens[b]), any order, a repeated position
+ * counts as two keys, no causal mask; topk_len[b] == 0 gives out = 0 and
+ * lse = -inf). This is the sparse MLA step that follows an indexer's top-k in
+ * the GLM-5.2-FP8 decode article (tahou.com: summary; related-work paragraph
+ * on TileRT gathering the sparse KV rows by the top-2048 indices), run through
+ * the same Stream-K split and just-in-time merge: build the plan with the
+ * planner over topk_len (as the per-request lengths), kv heads = 1. The kernel
+ * gathers each listed latent row (576 bf16, row stride shape->v_row_stride)
+ * with 16-byte copies. shape->kind must be SKD_KIND_MLA (else SKD_EUNSUPPORTED);
+ * other arguments, ownership and errors as skd_decode_attention; a listed
+ * position outside [0, seqlens[b]) sets SKD_DEVERR_INDEX (that key is then
+ * position 0), topk_len[b] > topk_stride sets SKD_DEVERR_SEQLEN. */
+int skd_decode_attention_sparse(const skd_shape_t *shape, const void *q, const void *kv_pages,
+                                const int32_t *page_table, const int32_t *seqlens, const int32_t *topk_idx,
+                                int topk_stride, const int32_t *topk_len, const void *plan_dev, int n_ctas,
+                                void *ws, size_t ws_bytes, void *out, float *lse, void *stream);
 
 /* Launch option (process-wide, default on): launch the attention kernel with
  * programmatic dependent launch, so that it can be scheduled while the

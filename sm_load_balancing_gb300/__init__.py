@@ -19,12 +19,13 @@ from typing import Optional, Tuple
 import torch
 
 from . import _native as N
-from ._native import (SKD_DEVERR_PAGE, SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN,
+from ._native import (SKD_DEVERR_INDEX, SKD_DEVERR_PAGE, SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN,
                       SKD_DEVERR_TIMEOUT, SKD_GRANULE, SkdError)
 
-__all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention", "read_error",
-           "sm_count", "default_ctas", "default_seg_cost", "make_shape", "set_pdl", "SkdError", "SKD_GRANULE", "SKD_DEVERR_PLAN",
-           "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT"]
+__all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention", "decode_attention_sparse",
+           "read_error", "sm_count", "default_ctas", "default_seg_cost", "make_shape", "set_pdl", "SkdError",
+           "SKD_GRANULE", "SKD_DEVERR_PLAN", "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT",
+           "SKD_DEVERR_INDEX"]
 
 _MODES = {"streamk": N.SKD_PLAN_STREAMK, "round_robin": N.SKD_PLAN_ROUND_ROBIN,
           "fixed_split": N.SKD_PLAN_FIXED_SPLIT}
@@ -180,6 +181,40 @@ def decode_attention(q, k_pages, v_pages, page_table, seqlens, plan_dev, ws, *, 
         ctypes.byref(shape), q.data_ptr(), k_pages.data_ptr(), vp.data_ptr(), page_table.data_ptr(),
         seqlens.data_ptr(), plan_dev.data_ptr(), n, ws.data_ptr(), ws.numel(), out.data_ptr(),
         lse.data_ptr(), _stream_ptr(stream)))
+    return out, lse
+
+
+def decode_attention_sparse(q, kv_pages, page_table, seqlens, topk_idx, topk_len, plan_dev, ws, *,
+                            scale: float, n_ctas: Optional[int] = None,
+                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                            shape: Optional[N.Shape] = None,
+                            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse (top-k) absorbed-MLA decode: request b attends only to the cache
+    positions ``topk_idx[b, :topk_len[b]]`` (int32 [B, K] and [B] on the
+    device). ``plan_dev`` must come from the planner run over ``topk_len``
+    (``plan(topk_len_host, 1, page_size, n)``). Returns (out, lse) like
+    ``decode_attention``."""
+    _chk(q, "q", torch.bfloat16)
+    _chk(kv_pages, "kv_pages", torch.bfloat16)
+    _chk(page_table, "page_table", torch.int32)
+    _chk(seqlens, "seqlens", torch.int32)
+    _chk(topk_idx, "topk_idx", torch.int32)
+    _chk(topk_len, "topk_len", torch.int32)
+    _chk(plan_dev, "plan", torch.int32)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != q.shape[0] or topk_len.numel() != q.shape[0]:
+        raise ValueError("topk_idx must be [B, K] and topk_len [B]")
+    if shape is None:
+        shape = make_shape(q, kv_pages, None, page_table, scale=scale, causal=False)
+    B, T, Hq = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    if out is None:
+        out = torch.empty(B, T, Hq, shape.head_dim_v, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, Hq, dtype=torch.float32, device=q.device)
+    n = int(plan_dev[3].item()) if n_ctas is None else int(n_ctas)
+    N.check("skd_decode_attention_sparse", N.lib().skd_decode_attention_sparse(
+        ctypes.byref(shape), q.data_ptr(), kv_pages.data_ptr(), page_table.data_ptr(), seqlens.data_ptr(),
+        topk_idx.data_ptr(), int(topk_idx.shape[1]), topk_len.data_ptr(), plan_dev.data_ptr(), n,
+        ws.data_ptr(), ws.numel(), out.data_ptr(), lse.data_ptr(), _stream_ptr(stream)))
     return out, lse
 
 

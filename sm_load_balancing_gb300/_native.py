@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libskdecode.so")
 SKD_OK, SKD_EINVAL, SKD_EUNSUPPORTED, SKD_ECUDA, SKD_EPLAN, SKD_ESIZE = range(6)
 SKD_KIND_GQA, SKD_KIND_MLA = 0, 1
 SKD_PLAN_STREAMK, SKD_PLAN_ROUND_ROBIN, SKD_PLAN_FIXED_SPLIT = 0, 1, 2
-SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN, SKD_DEVERR_PAGE, SKD_DEVERR_TIMEOUT = 1, 2, 4, 8
+SKD_DEVERR_PLAN, SKD_DEVERR_SEQLEN, SKD_DEVERR_PAGE, SKD_DEVERR_TIMEOUT, SKD_DEVERR_INDEX = 1, 2, 4, 8, 16
 SKD_GRANULE = 16
 
 # every symbol include/skdecode.h declares, with (restype, argtypes)
@@ -52,6 +52,8 @@ SIGNATURES = {
                                       _vp, _c_size, _vp, _vp, _vp]),
     "skd_decode_attention_noalloc": (_c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp,
                                               _c_int, _vp, _vp, _vp]),
+    "skd_decode_attention_sparse": (_c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _vp,
+                                             _c_int, _vp, _c_size, _vp, _vp, _vp]),
 }
 
 _lib = None

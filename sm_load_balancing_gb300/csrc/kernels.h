@@ -31,11 +31,14 @@ struct DecodeArgs {
   float *lse;
   cudaStream_t stream;
   bool defer_merge = false;  // splits only write their partial states (two-kernel comparator)
+  // sparse MLA: listed cache positions [batch][topk_stride] and list lengths (null: dense)
+  const int32_t *topk = nullptr, *topk_len = nullptr;
+  int topk_stride = 0;
 };
 
 int launch_gqa(const DecodeArgs &a);
 int launch_mla(const DecodeArgs &a);
-// MLA workers (3-CTA clusters) that can be resident at once on the current device
+// MLA workers (2-CTA clusters) that can be resident at once on the current device
 int mla_resident_workers(int *n);
 // the comparator's second kernel: merge every split item's partial states
 int launch_gqa_combine(const DecodeArgs &a);

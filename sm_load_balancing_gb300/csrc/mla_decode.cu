@@ -115,6 +115,14 @@ struct Params {
   int64_t slot_floats;
   long long *trace;
   int defer;  // 1: splits write their partial states and a combine kernel merges them
+  // sparse (top-k) attention: request b attends to the cache positions
+  // topk[b * topk_stride + i], i < topk_len[b] (the plan splits those lists);
+  // topk == nullptr: every position of the cache (dense)
+  const int32_t *topk;
+  const int32_t *topk_len;
+  int topk_stride;
+  const __nv_bfloat16 *kv;  // the latent cache, for the sparse row gather
+  int64_t kv_row_bytes;     // bytes between consecutive cache rows
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -150,6 +158,14 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
           dst_cluster),
       "r"(src), "r"(bytes), "r"(bar_cluster)
       : "memory");
+}
+// 16-byte global -> shared copy (L2 only) and the arrival that tracks this
+// thread's copies on a barrier (counted among the barrier's expected arrivals)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -383,9 +399,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cx.err = p.err;
   volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
 
+  // sparse: the 32 producer lanes gather a block's rows with cp.async, each
+  // arriving once on the stage's barrier (a Q fill: one expect_tx + 31 plain)
+  const bool sparse = p.topk != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNst; ++s) {
-      ptx::mbar_init(cx.bar(B_KVF + s), 1);
+      ptx::mbar_init(cx.bar(B_KVF + s), sparse ? 32 : 1);
       ptx::mbar_init(cx.bar(B_KVE + s), rank == 0 ? kQkIssuers : 1);
     }
     ptx::mbar_init(cx.bar(B_RE0), 1);
@@ -440,10 +459,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int b = sg.x, tb = sg.y, te = sg.z;
       if (te <= tb) continue;
       const int32_t *ptab = p.page_table + int64_t(b) * p.max_pages;
-      if (lane == 0) {
-        const int L = p.seqlens[b];
-        if (te > L || L > p.max_pages * p.P) atomicOr(p.err, SKD_DEVERR_SEQLEN);
-      }
+      const int L = p.seqlens[b];
+      const int len = sparse ? p.topk_len[b] : L;  // entries of the list the plan splits
+      if (lane == 0 && (te > len || L > p.max_pages * p.P || (sparse && len > p.topk_stride)))
+        atomicOr(p.err, SKD_DEVERR_SEQLEN);
       if (rank == 0) {
         // the segment's Q [128 heads][576] comes through the ring ahead of its
         // blocks, as fills of chunks 0-3, 4-7 and 8 (16 KB each); the issuers
@@ -462,11 +481,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (sparse && ok && lane != 0) ptx::mbar_arrive(cx.bar(B_KVF + s));
         }
       }
       for (int w0 = (tb / kBlk) * kBlk; w0 < te && ok; w0 += kBlk, ++g, ++m) {
         const int s = m % kNst;
         const uint32_t ph = uint32_t(m / kNst) & 1u;
+        if (sparse) {
+          // the block is list entries [w0, w0 + 64): each row (one listed
+          // position) is 1152 contiguous bytes, copied by the warp in 16-byte
+          // pieces straight into the 128-byte swizzled stage (rank 1: only
+          // the 1024 bytes of value columns). Entries past the list are not
+          // loaded: their scores are masked and rank 1 zeroes their V rows.
+          if (lane == 0)
+            ok = (rank == 0 || g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
+                 (rank == 1 || cx.wait(B_RE0 + (g & 1), uint32_t((g >> 1) & 1) ^ 1u));
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          const int32_t *sel = p.topk + int64_t(b) * p.topk_stride;
+          auto resolve = [&](int e) -> int64_t {  // cache row of list entry e, or -1
+            if (e >= len || e >= p.topk_stride) return -1;
+            int j = __ldg(sel + e);
+            if (j < 0 || j >= L) {
+              atomicOr(p.err, SKD_DEVERR_INDEX);
+              j = 0;
+            }
+            int pg = j / p.P < p.max_pages ? __ldg(ptab + j / p.P) : -1;
+            if (pg < 0 || pg >= p.num_pages) {
+              atomicOr(p.err, SKD_DEVERR_PAGE);
+              pg = 0;
+              j = 0;
+            }
+            return int64_t(pg) * p.P + j % p.P;
+          };
+          const int64_t ra = resolve(w0 + lane), rb = resolve(w0 + 32 + lane);
+          const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
+          const uint32_t rope = cx.sbase + kOffRope + (g & 1) * kChunkBytes;
+          const int npc = rank == 0 ? kDk / 8 : kDv / 8;  // 16-byte pieces per row
+          for (int t = 0; t < kBlk; ++t) {
+            const int64_t r = __shfl_sync(0xffffffffu, t < 32 ? ra : rb, t & 31);
+            if (r < 0) continue;  // warp-uniform
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.kv) + r * p.kv_row_bytes;
+            for (int pc = lane; pc < npc; pc += 32) {
+              const int c = pc >> 3, k16 = pc & 7;
+              cp_async16((c < 8 ? ring + c * kChunkBytes : rope) + uint32_t(t) * 128 + uint32_t((k16 ^ (t & 7)) << 4),
+                         src + pc * 16);
+            }
+          }
+          cp_async_arrive_noinc(cx.bar(B_KVF + s));
+          if (lane == 0) misc[3] = uint32_t(m + 1);
+          continue;
+        }
         if (lane == 0) {
           const int j = w0 / p.P;
           int pg = j < p.max_pages ? __ldg(ptab + j) : -1;
@@ -529,6 +594,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
+            // a gathered block was written by cp.async (generic proxy); the MMAs read it (async proxy)
+            if (sparse) ptx::fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
             const uint32_t rope = cx.sbase + kOffRope + (g & 1) * kChunkBytes;
@@ -557,6 +624,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
+            if (sparse) ptx::fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
             const uint32_t pbuf = cx.sbase + kOffP + pb * kPBytes;
@@ -733,7 +801,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (hc == 0) p.lse[orow] = -INFINITY;
         continue;
       }
-      const int L = p.seqlens[b];
+      const int L = sparse ? p.topk_len[b] : p.seqlens[b];  // entries of the list (positions when dense)
       const int nb = num_blocks(tb, te);
       for (int j = 0; j < nb; ++j, ++g) {
         const int w0 = (tb / kBlk) * kBlk + j * kBlk;
@@ -1149,6 +1217,11 @@ int launch_mla(const DecodeArgs &a) {
   p.slot_floats = a.wl.slot_floats;
   p.trace = static_cast<long long *>(trace_buffer(2 * a.n_ctas));
   p.defer = a.defer_merge ? 1 : 0;
+  p.topk = a.topk;
+  p.topk_len = a.topk_len;
+  p.topk_stride = a.topk_stride;
+  p.kv = static_cast<const __nv_bfloat16 *>(a.k);
+  p.kv_row_bytes = int64_t(s.v_row_stride) * 2;
   if (set_smem_attr() != SKD_OK) return SKD_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.n_ctas);

@@ -249,6 +249,42 @@ int skd_decode_attention_split_combine(const skd_shape_t *shape, const void *q, 
                        lse, stream, true);
 }
 
+int skd_decode_attention_sparse(const skd_shape_t *shape, const void *q, const void *kv_pages,
+                                const int32_t *page_table, const int32_t *seqlens, const int32_t *topk_idx,
+                                int topk_stride, const int32_t *topk_len, const void *plan_dev, int n_ctas,
+                                void *ws, size_t ws_bytes, void *out, float *lse, void *stream) {
+  const int st = validate_shape(shape);
+  if (st != SKD_OK) return st;
+  if (shape->kind != SKD_KIND_MLA) return SKD_EUNSUPPORTED;
+  if (n_ctas < 1 || topk_stride < 1) return SKD_EINVAL;
+  if (shape->batch == 0) return SKD_OK;
+  if (!q || !kv_pages || !page_table || !seqlens || !topk_idx || !topk_len || !plan_dev || !ws || !out || !lse)
+    return SKD_EINVAL;
+  if (!aligned(q, 16) || !aligned(kv_pages, 16) || !aligned(out, 16) || !aligned(plan_dev, 16) ||
+      !aligned(ws, 256) || !aligned(page_table, 4) || !aligned(seqlens, 4) || !aligned(topk_idx, 4) ||
+      !aligned(topk_len, 4) || !aligned(lse, 4))
+    return SKD_EINVAL;
+  DecodeArgs a;
+  a.shape = *shape;
+  a.q = q;
+  a.k = kv_pages;
+  a.v = kv_pages;
+  a.page_table = page_table;
+  a.seqlens = seqlens;
+  a.plan = static_cast<const int32_t *>(plan_dev);
+  a.n_ctas = n_ctas;
+  a.ws = ws;
+  a.wl = ws_layout(*shape, n_ctas);
+  if (ws_bytes < size_t(a.wl.bytes)) return SKD_ESIZE;
+  a.out = out;
+  a.lse = lse;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.topk = topk_idx;
+  a.topk_len = topk_len;
+  a.topk_stride = topk_stride;
+  return launch_mla(a);
+}
+
 int skd_set_pdl(int enable) {
   g_pdl = enable != 0;
   return SKD_OK;
