@@ -121,8 +121,6 @@ struct Params {
   const int32_t *topk;
   const int32_t *topk_len;
   int topk_stride;
-  const __nv_bfloat16 *kv;  // the latent cache, for the sparse row gather
-  int64_t kv_row_bytes;     // bytes between consecutive cache rows
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -159,13 +157,15 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
       "r"(src), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
-// 16-byte global -> shared copy (L2 only) and the arrival that tracks this
-// thread's copies on a barrier (counted among the barrier's expected arrivals)
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+// four listed rows x one 64-column box of a 2-D map (one row high) into 512
+// consecutive bytes of shared memory, swizzled like a 4-row slice of a tile
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *m, uint32_t bar, int col, int r0, int r1,
+                                            int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -365,7 +365,8 @@ __device__ __forceinline__ int num_blocks(int tb, int te) { return (te + kBlk - 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmain, const __grid_constant__ CUtensorMap trope,
                       const __grid_constant__ CUtensorMap tpart, const __grid_constant__ CUtensorMap tout,
-                      const __grid_constant__ CUtensorMap tq, const Params p) {
+                      const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg,
+                      const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // with programmatic dependent launch this grid may start before the previous
   // kernel of the stream (e.g. the device planner) has finished: wait for it
@@ -399,12 +400,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cx.err = p.err;
   volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
 
-  // sparse: the 32 producer lanes gather a block's rows with cp.async, each
-  // arriving once on the stage's barrier (a Q fill: one expect_tx + 31 plain)
   const bool sparse = p.topk != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNst; ++s) {
-      ptx::mbar_init(cx.bar(B_KVF + s), sparse ? 32 : 1);
+      ptx::mbar_init(cx.bar(B_KVF + s), 1);
       ptx::mbar_init(cx.bar(B_KVE + s), rank == 0 ? kQkIssuers : 1);
     }
     ptx::mbar_init(cx.bar(B_RE0), 1);
@@ -481,26 +480,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (sparse && ok && lane != 0) ptx::mbar_arrive(cx.bar(B_KVF + s));
         }
       }
       for (int w0 = (tb / kBlk) * kBlk; w0 < te && ok; w0 += kBlk, ++g, ++m) {
         const int s = m % kNst;
         const uint32_t ph = uint32_t(m / kNst) & 1u;
         if (sparse) {
-          // the block is list entries [w0, w0 + 64): each row (one listed
-          // position) is 1152 contiguous bytes, copied by the warp in 16-byte
-          // pieces straight into the 128-byte swizzled stage (rank 1: only
-          // the 1024 bytes of value columns). Entries past the list are not
-          // loaded: their scores are masked and rank 1 zeroes their V rows.
-          if (lane == 0)
+          // the block is list entries [w0, w0 + 64): tile::gather4 TMA copies
+          // bring 4 listed cache rows x 64 columns per op into the 128-byte
+          // swizzled stage (16 ops per column chunk, lane c issuing chunk c;
+          // rank 1 only the 8 value chunks). Entries past the list read row 0
+          // of the cache: their scores are masked and rank 1 zeroes their V rows.
+          if (lane == 0) {
             ok = (rank == 0 || g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
                  (rank == 1 || cx.wait(B_RE0 + (g & 1), uint32_t((g >> 1) & 1) ^ 1u));
+            if (ok)
+              ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), rank == 0 ? kMainBytes + kChunkBytes : kMainBytes);
+          }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           const int32_t *sel = p.topk + int64_t(b) * p.topk_stride;
-          auto resolve = [&](int e) -> int64_t {  // cache row of list entry e, or -1
-            if (e >= len || e >= p.topk_stride) return -1;
+          auto resolve = [&](int e) -> int {  // cache row of list entry e (row 0 past the list)
+            if (e >= len || e >= p.topk_stride) return 0;
             int j = __ldg(sel + e);
             if (j < 0 || j >= L) {
               atomicOr(p.err, SKD_DEVERR_INDEX);
@@ -512,23 +513,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               pg = 0;
               j = 0;
             }
-            return int64_t(pg) * p.P + j % p.P;
+            return pg * p.P + j % p.P;
           };
-          const int64_t ra = resolve(w0 + lane), rb = resolve(w0 + 32 + lane);
+          const int ra = resolve(w0 + lane), rb = resolve(w0 + 32 + lane);
           const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
           const uint32_t rope = cx.sbase + kOffRope + (g & 1) * kChunkBytes;
-          const int npc = rank == 0 ? kDk / 8 : kDv / 8;  // 16-byte pieces per row
-          for (int t = 0; t < kBlk; ++t) {
-            const int64_t r = __shfl_sync(0xffffffffu, t < 32 ? ra : rb, t & 31);
-            if (r < 0) continue;  // warp-uniform
-            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.kv) + r * p.kv_row_bytes;
-            for (int pc = lane; pc < npc; pc += 32) {
-              const int c = pc >> 3, k16 = pc & 7;
-              cp_async16((c < 8 ? ring + c * kChunkBytes : rope) + uint32_t(t) * 128 + uint32_t((k16 ^ (t & 7)) << 4),
-                         src + pc * 16);
+          const int nch = rank == 0 ? 9 : 8;
+#pragma unroll 1
+          for (int i = 0; i < kBlk / 4; ++i) {
+            int r4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int t = 4 * i + u;
+              r4[u] = __shfl_sync(0xffffffffu, t < 32 ? ra : rb, t & 31);
             }
+            if (lane < nch)
+              tma_gather4((lane < 8 ? ring + lane * kChunkBytes : rope) + uint32_t(i) * 512, &tg, cx.bar(B_KVF + s),
+                          lane * 64, r4[0], r4[1], r4[2], r4[3]);
           }
-          cp_async_arrive_noinc(cx.bar(B_KVF + s));
           if (lane == 0) misc[3] = uint32_t(m + 1);
           continue;
         }
@@ -594,8 +596,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            // a gathered block was written by cp.async (generic proxy); the MMAs read it (async proxy)
-            if (sparse) ptx::fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
             const uint32_t rope = cx.sbase + kOffRope + (g & 1) * kChunkBytes;
@@ -624,7 +624,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            if (sparse) ptx::fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
             const uint32_t pbuf = cx.sbase + kOffP + pb * kPBytes;
@@ -1162,7 +1161,7 @@ int launch_mla(const DecodeArgs &a) {
   const skd_shape_t &s = a.shape;
   if (s.page_size % kBlk != 0) return SKD_EUNSUPPORTED;  // 64-token blocks must not straddle pages
   // latent cache viewed as {64 columns, rows (page*P + slot), 9 column chunks}
-  CUtensorMap tmain, trope, tpart, tout, tq;
+  CUtensorMap tmain, trope, tpart, tout, tq, tg;
   const cuuint64_t gk[3] = {64, cuuint64_t(s.num_pages) * s.page_size, 9};
   const cuuint64_t sk[2] = {cuuint64_t(s.v_row_stride) * 2, 128};
   const cuuint32_t es[3] = {1, 1, 1};
@@ -1172,6 +1171,15 @@ int launch_mla(const DecodeArgs &a) {
       encode_tiled(&trope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k), gk, sk, brope, es,
                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return SKD_EINVAL;
+  // sparse gather: the latent cache as 2-D rows {576 columns, rows}, boxes one row high x 64 columns
+  {
+    const cuuint64_t gg[2] = {cuuint64_t(kDk), cuuint64_t(s.num_pages) * s.page_size};
+    const cuuint64_t sg[1] = {cuuint64_t(s.v_row_stride) * 2};
+    const cuuint32_t bg[2] = {64, 1};
+    if (encode_tiled(&tg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.k), gg, sg, bg, es,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return SKD_EINVAL;
+  }
   // queries [batch * 128 heads][576] viewed as {64 columns, rows, 9 column chunks}, one chunk per box
   {
     const cuuint64_t gq[3] = {64, cuuint64_t(s.batch) * kHeads, 9};
@@ -1220,8 +1228,7 @@ int launch_mla(const DecodeArgs &a) {
   p.topk = a.topk;
   p.topk_len = a.topk_len;
   p.topk_stride = a.topk_stride;
-  p.kv = static_cast<const __nv_bfloat16 *>(a.k);
-  p.kv_row_bytes = int64_t(s.v_row_stride) * 2;
+
   if (set_smem_attr() != SKD_OK) return SKD_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.n_ctas);
@@ -1233,7 +1240,7 @@ int launch_mla(const DecodeArgs &a) {
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, tmain, trope, tpart, tout, tq, p) != cudaSuccess) return SKD_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, tmain, trope, tpart, tout, tq, tg, p) != cudaSuccess) return SKD_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 
