@@ -321,8 +321,19 @@ def run_ours(a):
 
     two_kernel = a.mode == "fixed_split"
 
+    prefix = None
+    if w.prefix_groups:
+        # shared-prefix decode: prefix pass + suffix pass + merge (4 launches of ours per step)
+        from sm_load_balancing_gb300.prefix import SharedPrefixDecode
+        if a.mode != "streamk" or sparse:
+            raise SystemExit("shared-prefix decode runs the Stream-K plans only")
+        prefix = SharedPrefixDecode(q, k, v, w.page_table, w.seqlens, w.prefix_groups, w.prefix_lens,
+                                    scale=w.scale, causal=w.causal, n_ctas=n)
+
     def step():
-        if sparse:
+        if prefix is not None:
+            prefix(q, out=out, lse=lse, stream=stream)
+        elif sparse:
             skd.decode_attention_sparse(q, k, pt, sl, ti, tl, plan_d, ws, scale=w.scale, n_ctas=n, out=out,
                                         lse=lse, shape=shape, stream=stream)
         else:
@@ -371,6 +382,25 @@ def run_ours(a):
     if err != 0:
         raise RuntimeError(f"device error word {err}")
     launch = _launch_study(skd, q, k, v, pt, sl, w, shape, n, seg_cost, ws, out, lse, a) if a.launch_study else None
+    if prefix is not None:
+        for wsx in prefix.workspaces():
+            if skd.read_error(wsx) != 0:
+                raise RuntimeError(f"device error word {skd.read_error(wsx)}")
+        # context: the plain decode of the full sequences reads every prefix once per request
+        ref_us = []
+        for _ in range(max(3, min(a.steps, 50))):
+            if flush is not None:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            skd.decode_attention(q, k, v, pt, sl, plan_d, ws, scale=w.scale, causal=w.causal, n_ctas=n,
+                                 out=out, lse=lse, shape=shape, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ref_us.append(e0.elapsed_time(e1) * 1e3)
+        prefix_ctx = {"plain_decode_us": statistics.median(ref_us[2:] or ref_us),
+                      "plain_decode_kv_tokens": int(w.seqlens.astype("int64").sum()),
+                      "virtual_prefix_requests": prefix.V, "requests_per_virtual": prefix.R}
 
     if world > 1:
         import torch.distributed as dist
@@ -407,7 +437,9 @@ def run_ours(a):
             pt_d.copy_(pt_h, non_blocking=True)
             sl_d.copy_(sl_h, non_blocking=True)
             plan_dd.copy_(plan_pin, non_blocking=True)
-            if sparse:
+            if prefix is not None:
+                prefix(q_d, out=out, lse=lse, stream=stream)
+            elif sparse:
                 ti_d.copy_(ti_h, non_blocking=True)
                 tl_d.copy_(tl_h, non_blocking=True)
                 skd.decode_attention_sparse(q_d, k, pt_d, sl_d, ti_d, tl_d, plan_dd, ws, scale=w.scale, n_ctas=n,
@@ -441,7 +473,9 @@ def run_ours(a):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "us_per_step": t_e2e * 1e6, "steps": n_e2e,
                "note": "host planner + pinned H2D of q/seqlens/page table/plan" + ("/top-k lists" if sparse else "")
-                       + " + kernel + D2H of out/lse; KV cache resident"}
+                       + " + kernel + D2H of out/lse; KV cache resident"
+                       + ("; shared prefix: its layouts and plans are prepared once, outside the loop"
+                          if prefix is not None else "")}
         if skd.read_error(ws) != 0:
             raise RuntimeError("device error in e2e loop")
 
@@ -463,11 +497,15 @@ def run_ours(a):
                      "kernel": f"{kind}_decode_kernel", "launch_ms_mean": mean_kernel_ms,
                      "launch_ms_median": statistics.median(per)},
         "e2e": e2e,
-        "gpu_launches": a.steps * (2 if two_kernel else 1),
+        "gpu_launches": a.steps * (prefix.launches() if prefix is not None else 2 if two_kernel else 1),
         "clocks": ck,
     }
     if launch is not None:
         line["launch"] = launch
+    if prefix is not None:
+        line["shared_prefix"] = prefix_ctx
+        line["roofline"]["kernel"] = ("shared-prefix step (gather + gqa_decode + merge)" if prefix.fused else
+                                      "shared-prefix step (gqa_decode x2 + gather + merge)")
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         try:
             bps, cores, desc, dt = _cpu_oracle_sample(w, a.cpu_seconds)

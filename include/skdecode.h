@@ -201,6 +201,32 @@ int skd_decode_attention_sparse(const skd_shape_t *shape, const void *q, const v
                                 int topk_stride, const int32_t *topk_len, const void *plan_dev, int n_ctas,
                                 void *ws, size_t ws_bytes, void *out, float *lse, void *stream);
 
+/* ---- composing decode launches (shared-prefix decode) ------------------ */
+
+/* dst row i = src row src_rows[i] for i < n_rows, a row of zeros where
+ * src_rows[i] < 0. Rows are row_bytes long (a multiple of 16); dst and src
+ * 16-byte aligned, src_rows int32 on the device. Used to stack the query rows
+ * of requests that share a prefix into one virtual request. Asynchronous on
+ * `stream`; errors: SKD_EINVAL (sizes, null or misaligned pointers), SKD_ECUDA. */
+int skd_gather_rows(void *dst, const void *src, const int32_t *src_rows, int64_t n_rows, int64_t row_bytes,
+                    void *stream);
+
+/* Merge two attention results of the same query rows over disjoint key sets
+ * A and B (the reduction of partial states in "MeldKernel：动态负载下跨 SM 融合内核
+ * （SOSP 2026）", core method; used for its shared-prefix decode, Fig. 11):
+ * with M = max(lse_A, lse_B), w_X = exp(lse_X - M):
+ *   out = (w_A out_A + w_B out_B) / (w_A + w_B),  lse = M + ln(w_A + w_B),
+ * lse in natural-log units as skd_decode_attention writes it; both empty
+ * (lse = -inf) gives out = 0, lse = -inf. Row r of the result takes state A
+ * from row a_rows[r] of out_a / lse_a and state B from row b_rows[r] of
+ * out_b / lse_b (a negative entry: no such state; a NULL map: row r). out
+ * rows are bf16 [n_rows][head_dim_v] (head_dim_v a multiple of 8), lse fp32;
+ * out / lse may be out_b / lse_b when b_rows is NULL. Asynchronous; errors:
+ * SKD_EINVAL, SKD_ECUDA. */
+int skd_merge_states(const void *out_a, const float *lse_a, const int32_t *a_rows, const void *out_b,
+                     const float *lse_b, const int32_t *b_rows, void *out, float *lse, int64_t n_rows,
+                     int head_dim_v, void *stream);
+
 /* Launch option (process-wide, default on): launch the attention kernel with
  * programmatic dependent launch, so that it can be scheduled while the
  * previous kernel of the stream (typically skd_decode_plan_device, which

@@ -54,6 +54,8 @@ SIGNATURES = {
                                               _c_int, _vp, _vp, _vp]),
     "skd_decode_attention_sparse": (_c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _vp,
                                              _c_int, _vp, _c_size, _vp, _vp, _vp]),
+    "skd_gather_rows": (_c_int, [_vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64, _vp]),
+    "skd_merge_states": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _c_int, _vp]),
 }
 
 _lib = None

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libskdecode.so")
-SOURCES = ["skd_api.cu", "gqa_decode.cu", "mla_decode.cu", "plan_device.cu", "plan_host.cpp"]
+SOURCES = ["skd_api.cu", "gqa_decode.cu", "mla_decode.cu", "plan_device.cu", "plan_host.cpp", "compose.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -43,6 +43,13 @@ int mla_resident_workers(int *n);
 // the comparator's second kernel: merge every split item's partial states
 int launch_gqa_combine(const DecodeArgs &a);
 int launch_mla_combine(const DecodeArgs &a);
+// compose.cu: dst row i = src row src_rows[i] (zeros for a negative index)
+int launch_gather_rows(void *dst, const void *src, const int32_t *src_rows, int64_t n_rows, int64_t row_bytes,
+                       cudaStream_t stream);
+// compose.cu: merge two attention results (out bf16, lse) over disjoint key sets, row by row
+int launch_merge_states(const void *out_a, const float *lse_a, const int32_t *a_rows, const void *out_b,
+                        const float *lse_b, const int32_t *b_rows, void *out, float *lse, int64_t n_rows,
+                        int head_dim_v, cudaStream_t stream);
 int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n_ctas, int seg_cost, int32_t *plan,
                        cudaStream_t stream);
 

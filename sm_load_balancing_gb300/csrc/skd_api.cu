@@ -285,6 +285,28 @@ int skd_decode_attention_sparse(const skd_shape_t *shape, const void *q, const v
   return launch_mla(a);
 }
 
+int skd_gather_rows(void *dst, const void *src, const int32_t *src_rows, int64_t n_rows, int64_t row_bytes,
+                    void *stream) {
+  if (n_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return SKD_EINVAL;
+  if (n_rows == 0) return SKD_OK;
+  if (!dst || !src || !src_rows || !aligned(dst, 16) || !aligned(src, 16) || !aligned(src_rows, 4))
+    return SKD_EINVAL;
+  return launch_gather_rows(dst, src, src_rows, n_rows, row_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int skd_merge_states(const void *out_a, const float *lse_a, const int32_t *a_rows, const void *out_b,
+                     const float *lse_b, const int32_t *b_rows, void *out, float *lse, int64_t n_rows,
+                     int head_dim_v, void *stream) {
+  if (n_rows < 0 || head_dim_v <= 0 || head_dim_v % 8 != 0) return SKD_EINVAL;
+  if (n_rows == 0) return SKD_OK;
+  if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse || !aligned(out_a, 16) || !aligned(out_b, 16) ||
+      !aligned(out, 16) || !aligned(lse_a, 4) || !aligned(lse_b, 4) || !aligned(lse, 4) ||
+      (a_rows && !aligned(a_rows, 4)) || (b_rows && !aligned(b_rows, 4)))
+    return SKD_EINVAL;
+  return launch_merge_states(out_a, lse_a, a_rows, out_b, lse_b, b_rows, out, lse, n_rows, head_dim_v,
+                             static_cast<cudaStream_t>(stream));
+}
+
 int skd_set_pdl(int enable) {
   g_pdl = enable != 0;
   return SKD_OK;

@@ -36,6 +36,7 @@ __all__ = [
     "make",
     "make_custom",
     "select_topk",
+    "share_prefix",
     "fp32_to_bf16_bits",
     "bf16_bits_to_fp32",
 ]
@@ -93,6 +94,8 @@ class Workload:
     seed: int = 0
     topk_idx: Optional[np.ndarray] = None  # int32 [B][K]: listed cache positions (sparse attention)
     topk_len: Optional[np.ndarray] = None  # int32 [B]: entries of row b that are listed
+    prefix_groups: Optional[list] = None   # lists of requests whose first pages are shared
+    prefix_lens: Optional[list] = None     # shared prefix length (tokens) of each group
 
     @property
     def sparse(self) -> bool:
@@ -113,10 +116,14 @@ class Workload:
 
     @property
     def kv_tokens(self) -> int:
-        """KV rows the attention reads: all cached tokens, or the listed ones."""
+        """KV rows the attention reads: all cached tokens, or the listed ones;
+        with shared prefixes, each group's prefix once."""
         if self.sparse:
             return int(self.topk_len.astype(np.int64).sum())
-        return int(self.seqlens.astype(np.int64).sum())
+        n = int(self.seqlens.astype(np.int64).sum())
+        if self.prefix_groups:
+            n -= sum((len(g) - 1) * int(lp) for g, lp in zip(self.prefix_groups, self.prefix_lens))
+        return n
 
     def kv_bytes_per_token(self) -> int:
         if self.mla:
@@ -131,6 +138,8 @@ class Workload:
             pages = 2 * self.kv_tokens
         else:
             pages = int(sum((int(L) + P - 1) // P for L in self.seqlens))
+            if self.prefix_groups:
+                pages -= sum((len(g) - 1) * int(lp) // P for g, lp in zip(self.prefix_groups, self.prefix_lens))
         rows = self.batch * self.q_tokens * self.num_q_heads
         return (self.kv_tokens * self.kv_bytes_per_token()
                 + rows * self.head_dim_qk * 2 + rows * self.head_dim_v * 2 + rows * 4 + pages * 4)
@@ -151,7 +160,9 @@ class Workload:
                     head_dim_qk=self.head_dim_qk, head_dim_v=self.head_dim_v,
                     page_size=self.page_size, causal=self.causal, mla=self.mla,
                     kv_tokens=self.kv_tokens, seed=self.seed,
-                    **({"topk": int(self.topk_idx.shape[1])} if self.sparse else {}))
+                    **({"topk": int(self.topk_idx.shape[1])} if self.sparse else {}),
+                    **({"prefix_groups": [len(g) for g in self.prefix_groups],
+                        "prefix_lens": [int(x) for x in self.prefix_lens]} if self.prefix_groups else {}))
 
 
 def _assemble(name, rng, seqlens, *, T, Hq, Hkv, Dk, Dv, P, causal, scale, mla, seed,
@@ -226,6 +237,32 @@ def select_topk(w: Workload, k: int, seed: Optional[int] = None, name: Optional[
     return dataclasses.replace(w, topk_idx=idx, topk_len=n, name=name or w.name + f"_top{k}")
 
 
+def share_prefix(w: Workload, groups, prefix_lens, name: Optional[str] = None) -> Workload:
+    """The same batch where each group's requests share their first
+    prefix_len tokens: every member's page table lists the first member's
+    pages for them (the members' own prefix pages are left unused)."""
+    pt = w.page_table.copy()
+    for g, lp in zip(groups, prefix_lens):
+        npg = int(lp) // w.page_size
+        assert int(lp) % w.page_size == 0 and all(int(w.seqlens[b]) >= int(lp) for b in g)
+        for b in g[1:]:
+            pt[b, :npg] = pt[g[0], :npg]
+    return dataclasses.replace(w, page_table=pt, prefix_groups=[list(g) for g in groups],
+                               prefix_lens=[int(x) for x in prefix_lens], name=name or w.name + "_shared")
+
+
+def _shared_prefix(seed):
+    """Llama-3-8B-shaped GQA decode, 8 groups of 4 requests sharing a
+    4096-token prefix (a system prompt / few-shot context), own suffixes
+    U[64, 1024]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    suffix = rng.integers(64, 1024, size=32, endpoint=True)
+    w = _assemble("shared_prefix_gqa", rng, 4096 + suffix, T=1, Hq=32, Hkv=8, Dk=128, Dv=128, P=16,
+                  causal=False, scale=1.0 / math.sqrt(128), mla=False, seed=seed)
+    groups = [list(range(4 * i, 4 * i + 4)) for i in range(8)]
+    return share_prefix(w, groups, [4096] * 8, name="shared_prefix_gqa_b32_8x4_p4096_h32kv8_d128_p16")
+
+
 def _mla_sparse(seed):
     return select_topk(_mla(seed), 2048, name="mla_sparse_top2048_b64_h128_d576v512_p64")
 
@@ -245,6 +282,7 @@ WORKLOADS = {
     "mla_absorbed": _mla,
     "speculative_gqa": _speculative,
     "mla_sparse_top2048": _mla_sparse,
+    "shared_prefix_gqa": _shared_prefix,
 }
 
 
@@ -283,6 +321,8 @@ def draw_seqlens(name: str, seed: int = 0) -> np.ndarray:
         return np.insert(short, pos, 131072).astype(np.int32)
     if name in ("mla_absorbed", "mla_sparse_top2048"):
         return rng.integers(1024, 16384, size=64, endpoint=True).astype(np.int32)
+    if name == "shared_prefix_gqa":
+        return (4096 + rng.integers(64, 1024, size=32, endpoint=True)).astype(np.int32)
     if name == "speculative_gqa":
         return rng.integers(4096, 32768, size=16, endpoint=True).astype(np.int32)
     raise KeyError(name)
