@@ -158,13 +158,23 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
       : "memory");
 }
 // four listed rows x one 64-column box of a 2-D map (one row high) into 512
-// consecutive bytes of shared memory, swizzled like a 4-row slice of a tile
+// consecutive bytes of shared memory, swizzled like a 4-row slice of a tile;
+// with a CTA mask, into the same offset of every CTA of the mask, completing
+// on the barrier at the same offset in each
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *m, uint32_t bar, int col, int r0, int r1,
                                             int r2, int r3) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar, int col, int r0,
+                                               int r1, int r2, int r3, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -305,6 +315,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tma3_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2,
+                                        uint16_t mask, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2,
                                      uint64_t pol) {
   asm volatile(
@@ -404,7 +422,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNst; ++s) {
       ptx::mbar_init(cx.bar(B_KVF + s), 1);
-      ptx::mbar_init(cx.bar(B_KVE + s), rank == 0 ? kQkIssuers : 1);
+      // sparse: one ring shared by the pair (every fill lands in both CTAs),
+      // so a stage is free once the 3 score issuers and the PV issuer are done
+      ptx::mbar_init(cx.bar(B_KVE + s), sparse ? kQkIssuers + 1 : rank == 0 ? kQkIssuers : 1);
     }
     ptx::mbar_init(cx.bar(B_RE0), 1);
     ptx::mbar_init(cx.bar(B_RE0 + 1), 1);
@@ -462,10 +482,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int len = sparse ? p.topk_len[b] : L;  // entries of the list the plan splits
       if (lane == 0 && (te > len || L > p.max_pages * p.P || (sparse && len > p.topk_stride)))
         atomicOr(p.err, SKD_DEVERR_SEQLEN);
-      if (rank == 0) {
+      if (rank == 0 || sparse) {
         // the segment's Q [128 heads][576] comes through the ring ahead of its
         // blocks, as fills of chunks 0-3, 4-7 and 8 (16 KB each); the issuers
-        // copy it into TMEM
+        // copy it into TMEM. With the shared ring (sparse) the fills land in
+        // both CTAs, rank 1 only accounts for their bytes.
         for (int qb = 0; qb < 3 && ok; ++qb, ++m) {
           const int s = m % kNst;
           if (lane == 0) {
@@ -473,24 +494,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (ok) {
               const int nch = qb < 2 ? 4 : 1;
               ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), uint32_t(nch) * kQChunkBytes);
-              for (int c = 0; c < nch; ++c)
-                tma3(cx.sbase + kOffRing + s * kMainBytes + c * kQChunkBytes, &tq, cx.bar(B_KVF + s), 0,
-                     b * kHeads, 4 * qb + c, pol);
+              for (int c = 0; c < nch && rank == 0; ++c) {
+                const uint32_t dst = cx.sbase + kOffRing + s * kMainBytes + c * kQChunkBytes;
+                if (sparse)
+                  tma3_mc(dst, &tq, cx.bar(B_KVF + s), 0, b * kHeads, 4 * qb + c, 0x3, pol);
+                else
+                  tma3(dst, &tq, cx.bar(B_KVF + s), 0, b * kHeads, 4 * qb + c, pol);
+              }
               misc[3] = uint32_t(m + 1);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
       }
+      // sparse: the cache row of list entry e (row 0 past the list); each lane
+      // resolves two entries of a block, one block ahead of its gather, so the
+      // two dependent loads (list, page table) overlap the previous block
+      const int32_t *sel = sparse ? p.topk + int64_t(b) * p.topk_stride : nullptr;
+      auto resolve = [&](int e) -> int {
+        if (e >= len || e >= p.topk_stride) return 0;
+        int j = __ldg(sel + e);
+        if (j < 0 || j >= L) {
+          atomicOr(p.err, SKD_DEVERR_INDEX);
+          j = 0;
+        }
+        int pg = j / p.P < p.max_pages ? __ldg(ptab + j / p.P) : -1;
+        if (pg < 0 || pg >= p.num_pages) {
+          atomicOr(p.err, SKD_DEVERR_PAGE);
+          pg = 0;
+          j = 0;
+        }
+        return pg * p.P + j % p.P;
+      };
+      int next_a = 0, next_b = 0;
+      if (sparse) {
+        const int w = (tb / kBlk) * kBlk;
+        next_a = resolve(w + lane);
+        next_b = resolve(w + 32 + lane);
+      }
       for (int w0 = (tb / kBlk) * kBlk; w0 < te && ok; w0 += kBlk, ++g, ++m) {
         const int s = m % kNst;
         const uint32_t ph = uint32_t(m / kNst) & 1u;
         if (sparse) {
+          const int ra = next_a, rb = next_b;
+          if (w0 + kBlk < te) {
+            next_a = resolve(w0 + kBlk + lane);
+            next_b = resolve(w0 + kBlk + 32 + lane);
+          }
           // the block is list entries [w0, w0 + 64): tile::gather4 TMA copies
           // bring 4 listed cache rows x 64 columns per op into the 128-byte
-          // swizzled stage (16 ops per column chunk, lane c issuing chunk c;
-          // rank 1 only the 8 value chunks). Entries past the list read row 0
-          // of the cache: their scores are masked and rank 1 zeroes their V rows.
+          // swizzled stage (16 ops per column chunk, lane c issuing chunk c).
+          // The ring is shared: value chunks 0-3 come from rank 0 and 4-7 from
+          // rank 1, each multicast into both CTAs, and rank 0 alone loads the
+          // rope chunk, so each SM's TMA unit issues about half of the block.
+          // Entries past the list read row 0 of the cache: their scores are
+          // masked and rank 1 zeroes their V rows.
           if (lane == 0) {
             ok = (rank == 0 || g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
                  (rank == 1 || cx.wait(B_RE0 + (g & 1), uint32_t((g >> 1) & 1) ^ 1u));
@@ -499,26 +557,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
-          const int32_t *sel = p.topk + int64_t(b) * p.topk_stride;
-          auto resolve = [&](int e) -> int {  // cache row of list entry e (row 0 past the list)
-            if (e >= len || e >= p.topk_stride) return 0;
-            int j = __ldg(sel + e);
-            if (j < 0 || j >= L) {
-              atomicOr(p.err, SKD_DEVERR_INDEX);
-              j = 0;
-            }
-            int pg = j / p.P < p.max_pages ? __ldg(ptab + j / p.P) : -1;
-            if (pg < 0 || pg >= p.num_pages) {
-              atomicOr(p.err, SKD_DEVERR_PAGE);
-              pg = 0;
-              j = 0;
-            }
-            return pg * p.P + j % p.P;
-          };
-          const int ra = resolve(w0 + lane), rb = resolve(w0 + 32 + lane);
           const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
           const uint32_t rope = cx.sbase + kOffRope + (g & 1) * kChunkBytes;
-          const int nch = rank == 0 ? 9 : 8;
+          // this rank's chunks: rank 0 lanes 0-3 (+ lane 8: rope), rank 1 lanes 4-7
+          const bool mine = rank == 0 ? (lane < 4 || lane == 8) : (lane >= 4 && lane < 8);
 #pragma unroll 1
           for (int i = 0; i < kBlk / 4; ++i) {
             int r4[4];
@@ -527,9 +569,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int t = 4 * i + u;
               r4[u] = __shfl_sync(0xffffffffu, t < 32 ? ra : rb, t & 31);
             }
-            if (lane < nch)
-              tma_gather4((lane < 8 ? ring + lane * kChunkBytes : rope) + uint32_t(i) * 512, &tg, cx.bar(B_KVF + s),
-                          lane * 64, r4[0], r4[1], r4[2], r4[3]);
+            if (mine) {
+              if (lane < 8)
+                tma_gather4_mc(ring + lane * kChunkBytes + uint32_t(i) * 512, &tg, cx.bar(B_KVF + s), lane * 64, r4[0],
+                               r4[1], r4[2], r4[3], 0x3);
+              else
+                tma_gather4(rope + uint32_t(i) * 512, &tg, cx.bar(B_KVF + s), lane * 64, r4[0], r4[1], r4[2], r4[3]);
+            }
           }
           if (lane == 0) misc[3] = uint32_t(m + 1);
           continue;
@@ -588,7 +634,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) tmem_cp128(tmem + kTQ + c * 32 + kk * 8, sdesc(src + kk * 32, 16, 1024));
           }
-          for (int qb = 0; qb < 3; ++qb) umma_commit(cx.bar(B_KVE + (m + qb) % kNst));
+          for (int qb = 0; qb < 3; ++qb) {
+            if (sparse)
+              umma_commit_mc(cx.bar(B_KVE + (m + qb) % kNst), 0x3);
+            else
+              umma_commit(cx.bar(B_KVE + (m + qb) % kNst));
+          }
           m += 3;
           for (int j = 0; j < nb && ok; ++j, ++g, ++m) {
             const int s = m % kNst;
@@ -608,19 +659,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 umma_ts(dS, tmem + kTQ + c * 32 + kk * 8, sdesc(bc + kk * 32, 16, 1024), id_qk, (cc | kk) != 0);
             }
             umma_commit(cx.bar(B_SF0));
-            umma_commit(cx.bar(B_KVE + s));
+            if (sparse)
+              umma_commit_mc(cx.bar(B_KVE + s), 0x3);  // the stage is shared with rank 1
+            else
+              umma_commit(cx.bar(B_KVE + s));
             if (qi == 2) umma_commit(cx.bar(B_RE0 + (g & 1)));
           }
         }
       } else {
         constexpr uint32_t id_pv = idesc(kHeads, 256, 1);
+        int m = 0;  // ring fills: the blocks, and with the shared ring (sparse) rank 0's Q fills too
         for (int si = seg_lo; si < seg_hi && ok; ++si) {
           const int4 sg = segs[si];
           if (sg.z <= sg.y) continue;
           const int nb = num_blocks(sg.y, sg.z);
-          for (int j = 0; j < nb; ++j, ++g) {
-            const int s = g % kNst, pb = g & 1;
-            if (!cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u) || !cx.wait(B_OR0 + pb, uint32_t((g >> 1) & 1))) {
+          if (sparse) {
+            // the segment's three Q fills pass through this CTA's ring too: release them
+            for (int qb = 0; qb < 3 && ok; ++qb, ++m) {
+              ok = cx.wait(B_KVF + m % kNst, uint32_t(m / kNst) & 1u);
+              if (ok) umma_commit_mc(cx.bar(B_KVE + m % kNst), 0x3);
+            }
+          }
+          for (int j = 0; j < nb && ok; ++j, ++g, ++m) {
+            const int s = m % kNst, pb = g & 1;
+            if (!cx.wait(B_KVF + s, uint32_t(m / kNst) & 1u) || !cx.wait(B_OR0 + pb, uint32_t((g >> 1) & 1))) {
               ok = false;
               break;
             }
@@ -635,7 +697,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 umma_ss(tmem + kTO + h * 256, a, sdesc(ring + h * 4 * kChunkBytes + kk * (16 * 128), 8192, 1024),
                         id_pv, (j > 0 || kk > 0) ? 1u : 0u);
             }
-            umma_commit(cx.bar(B_KVE + s));
+            if (sparse)
+              umma_commit_mc(cx.bar(B_KVE + s), 0x3);  // the stage is shared with rank 0
+            else
+              umma_commit(cx.bar(B_KVE + s));
             umma_commit_mc(cx.bar(B_PVD0 + pb), 0x3);  // P buffer free (rank 0), O ready (rank 1)
           }
         }
@@ -788,7 +853,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile int *decision = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
     const uint32_t tOh = tmem + kTO + lane_off + 256 * hc;  // this thread's row, this half's columns
     const int col0 = 256 * hc;
-    int g = 0, stn = 0;
+    int g = 0, m = 0, stn = 0;  // blocks, ring fills (the shared ring also carries Q fills)
     bool ok = true;
     for (int si = seg_lo; si < seg_hi; ++si) {
       const int4 sg = segs[si];
@@ -802,9 +867,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int L = sparse ? p.topk_len[b] : p.seqlens[b];  // entries of the list (positions when dense)
       const int nb = num_blocks(tb, te);
-      for (int j = 0; j < nb; ++j, ++g) {
+      if (sparse) m += 3;
+      for (int j = 0; j < nb; ++j, ++g, ++m) {
         const int w0 = (tb / kBlk) * kBlk + j * kBlk;
-        const int pb = g & 1, s = g % kNst;
+        const int pb = g & 1, s = m % kNst;
         ok = ok && cx.wait(B_PF0 + pb, uint32_t((g >> 1) & 1));
         const volatile uint32_t *fa =
             reinterpret_cast<const volatile uint32_t *>(smem + kOffFa + (pb * 4 + q4) * kFaBytes);
@@ -827,7 +893,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (w0 + kBlk > L) {
           // V rows of the block past the end of the request hold arbitrary
           // bytes (0 * NaN would poison O): zero them in this rank's copy
-          ok = ok && cx.wait(B_KVF + s, uint32_t(g / kNst) & 1u);
+          // (with the shared ring this warp may be more fills ahead of the PV
+          // issuer than the ring is deep, because rank 0's Q fills sit between
+          // blocks: first wait until the stage's previous fill was released by
+          // every consumer, so that the parity test below can only be passed
+          // by this block's fill)
+          if (sparse && m >= kNst) ok = ok && cx.wait(B_KVE + s, uint32_t((m - kNst) / kNst) & 1u);
+          ok = ok && cx.wait(B_KVF + s, uint32_t(m / kNst) & 1u);
           const int t_lo = max(0, min(kBlk, L - w0));
           const int nrow = kBlk - t_lo;
           uint8_t *stg = smem + kOffRing + uint32_t(s) * kMainBytes;
