@@ -311,7 +311,8 @@ def run_ours(a):
     plan_lens = w.topk_len if sparse else w.seqlens  # the planner splits what each request reads
     shape = skd.make_shape(q, k, v, pt, scale=w.scale, causal=w.causal)
     n = a.n_ctas or skd.default_ctas(shape)
-    seg_cost = 0 if a.mode != "streamk" else (skd.default_seg_cost(shape) if a.seg_cost is None else a.seg_cost)
+    seg_cost = 0 if a.mode != "streamk" else (skd.default_seg_cost(shape, sparse=sparse) if a.seg_cost is None
+                                              else a.seg_cost)
     plan_h = skd.plan(plan_lens, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)
     plan_d = plan_h.to(dev)
     ws = skd.workspace(shape, n, dev)

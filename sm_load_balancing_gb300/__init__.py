@@ -57,14 +57,21 @@ def default_ctas(shape: Optional[N.Shape] = None, device: Optional[int] = None) 
 
 # Fixed per-segment cost of the absorbed-MLA kernel in granules of KV work:
 # loading a request's 128 query rows into TMEM and draining its 128x512
-# accumulator take about as long as this many granules of streaming.
+# accumulator cost a few microseconds, which the dense kernel streams as
+# roughly this many granules. The sparse (top-k) path gathers its rows and
+# spends about five times as long per granule, so the same cost is fewer
+# granules there.
 MLA_SEG_COST = 40
+MLA_SPARSE_SEG_COST = 8
 
 
-def default_seg_cost(shape: Optional[N.Shape] = None) -> int:
+def default_seg_cost(shape: Optional[N.Shape] = None, sparse: bool = False) -> int:
     """Per-segment cost (granules) the planner charges by default: the MLA
-    kernel pays a large fixed cost per segment, the GQA kernel a negligible one."""
-    return MLA_SEG_COST if (shape is not None and shape.kind == N.SKD_KIND_MLA) else 0
+    kernel pays a fixed cost per segment (``sparse``: plans over top-k lists),
+    the GQA kernel a negligible one."""
+    if shape is None or shape.kind != N.SKD_KIND_MLA:
+        return 0
+    return MLA_SPARSE_SEG_COST if sparse else MLA_SEG_COST
 
 
 def plan_bytes(batch: int, num_kv_heads: int, n_ctas: int) -> int:

@@ -22,7 +22,7 @@ def _run(w, n_ctas=None, d=None):
     ti = torch.from_numpy(w.topk_idx).cuda()
     tl = torch.from_numpy(w.topk_len).cuda()
     n = skd.default_ctas(d.shape) if n_ctas is None else n_ctas
-    plan = skd.plan(w.topk_len, 1, w.page_size, n, seg_cost=skd.default_seg_cost(d.shape)).cuda()
+    plan = skd.plan(w.topk_len, 1, w.page_size, n, seg_cost=skd.default_seg_cost(d.shape, sparse=True)).cuda()
     ws = skd.workspace(d.shape, n)
     out, lse = skd.decode_attention_sparse(d.q, d.k, d.pt, d.sl, ti, tl, plan, ws, scale=w.scale, n_ctas=n,
                                            shape=d.shape)
@@ -70,7 +70,8 @@ def test_listing_every_position_matches_dense_bits():
     d = Dev(ws_)
     so, sl, err = _run(ws_, d=d)
     assert err == 0
-    do, dl, err2, _ = d.run()
+    import sm_load_balancing_gb300 as skd
+    do, dl, err2, _ = d.run(seg_cost=skd.default_seg_cost(d.shape, sparse=True))  # the same plan
     assert err2 == 0
     assert torch.equal(so, do) and torch.equal(sl, dl)
 
