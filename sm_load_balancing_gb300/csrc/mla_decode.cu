@@ -43,6 +43,7 @@ namespace {
 
 constexpr int kHeads = 128, kDk = 576, kDv = 512, kBlk = 64;
 // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quarter),
+// (sparse, rank 1) warp 10 forwards its gathered half of each block to rank 0,
 // warps 10-11 (rank 0) two more MMA issuers: one thread issues a tcgen05.mma
 // about every 90-120 cycles whatever its size, so the 36 small score MMAs of a
 // block are spread over three issuing warps
@@ -66,14 +67,15 @@ constexpr uint32_t kOffRope = kNst * kMainBytes;   // rank 0: [2][8 KB] columns 
 constexpr uint32_t kOffStage = kOffRope + 2 * kChunkBytes;  // rank 0: P staging [4 warps][4 KB]
 constexpr uint32_t kOffP = kNst * kMainBytes;      // rank 1: P [2][128 rows][64 tok] bf16, SW128
 constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;  // mbarriers
-constexpr int kNumBar = 24;
+constexpr int kNumBar = 28;
 // per (P buffer, warp): 32 rescale factors + a flag word, padded to 144 bytes
 // (rank 0 stages its copy in the slots of P buffer 0)
 constexpr uint32_t kFaBytes = 144;
 constexpr uint32_t kOffFa = kOffBar + kNumBar * 8;
 constexpr uint32_t kOffStats = kOffFa + 8 * kFaBytes;  // rank 1: m, l, lf [3][128] fp32
 constexpr uint32_t kOffMisc = kOffStats + 3 * kHeads * 4;
-// misc words: 0 tmem base, 1 abort, 2 merge decision, 3 blocks issued by the producer
+// misc words: 0 tmem base, 1 abort, 2 merge decision, 3 blocks issued by the producer,
+// 4 (sparse, rank 1) per stage: bit s parity of the gather phases issued, bit 8+s any issued
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffStage + 4 * kQuarterP <= kOffBar, "P staging overlaps the barriers");
@@ -96,7 +98,8 @@ enum {
   B_OR0, B_OR1,         // rank 1: O rescaled / V tail zeroed, PV may run (4)
   B_STF,                // rank 1: segment statistics landed (4 remote)
   B_STE,                // rank 0: statistics buffer free (4 remote)
-  B_FIN,                // MMA drain before TMEM release
+  B_KVH,                // [kNst] sparse: this CTA's own gathers of a fill landed
+  B_FIN = B_KVH + kNst,  // MMA drain before TMEM release
   B_COUNT
 };
 static_assert(B_COUNT <= kNumBar, "barrier count");
@@ -158,23 +161,13 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
       : "memory");
 }
 // four listed rows x one 64-column box of a 2-D map (one row high) into 512
-// consecutive bytes of shared memory, swizzled like a 4-row slice of a tile;
-// with a CTA mask, into the same offset of every CTA of the mask, completing
-// on the barrier at the same offset in each
+// consecutive bytes of shared memory, swizzled like a 4-row slice of a tile
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *m, uint32_t bar, int col, int r0, int r1,
                                             int r2, int r3) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar, int col, int r0,
-                                               int r1, int r2, int r3, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -315,14 +308,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma3_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2,
-                                        uint16_t mask, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask), "l"(pol)
-      : "memory");
-}
 __device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2,
                                      uint64_t pol) {
   asm volatile(
@@ -345,6 +330,11 @@ struct Ctx {
   long long *tr;  // per-CTA trace record or null
   __device__ uint32_t bar(int i) const { return sbase + kOffBar + 8u * i; }
   __device__ uint32_t peer_addr(uint32_t local) const { return mapa(local, peer); }
+  // a ring fill has landed: its barrier, and with the shared ring (sparse)
+  // also this CTA's own part of it (parity of KVH's phase: hpar)
+  __device__ bool wait_fill(int s, uint32_t parity, bool shared_ring, uint32_t hpar) const {
+    return wait(B_KVF + s, parity) && (!shared_ring || wait(B_KVH + s, hpar));
+  }
   // bounded wait with cluster-scope acquire; on timeout flag both ranks
   __device__ bool wait(int i, uint32_t parity) const {
     const uint32_t b = bar(i);
@@ -380,6 +370,9 @@ struct Ctx {
 // number of 64-token blocks touched by the token range [tb, te)
 __device__ __forceinline__ int num_blocks(int tb, int te) { return (te + kBlk - 1) / kBlk - tb / kBlk; }
 
+// kSparse: the top-k form (blocks of listed rows, gathered); a template
+// parameter so that the dense kernel carries none of its code
+template <bool kSparse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmain, const __grid_constant__ CUtensorMap trope,
                       const __grid_constant__ CUtensorMap tpart, const __grid_constant__ CUtensorMap tout,
@@ -418,13 +411,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cx.err = p.err;
   volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
 
-  const bool sparse = p.topk != nullptr;
+  constexpr bool sparse = kSparse;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNst; ++s) {
       ptx::mbar_init(cx.bar(B_KVF + s), 1);
-      // sparse: one ring shared by the pair (every fill lands in both CTAs),
-      // so a stage is free once the 3 score issuers and the PV issuer are done
-      ptx::mbar_init(cx.bar(B_KVE + s), sparse ? kQkIssuers + 1 : rank == 0 ? kQkIssuers : 1);
+      // sparse: one ring shared by the pair (every block lands in both CTAs);
+      // rank 0's 3 score issuers and rank 1's PV issuer release a fill in
+      // both CTAs, and rank 1's forwarding warp in its own as well
+      ptx::mbar_init(cx.bar(B_KVE + s), sparse ? kQkIssuers + 1 + rank : rank == 0 ? kQkIssuers : 1);
     }
     ptx::mbar_init(cx.bar(B_RE0), 1);
     ptx::mbar_init(cx.bar(B_RE0 + 1), 1);
@@ -441,9 +435,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(cx.bar(B_OR1), 8);
     ptx::mbar_init(cx.bar(B_STF), 4);
     ptx::mbar_init(cx.bar(B_STE), 8);
+    for (int s = 0; s < kNst; ++s) ptx::mbar_init(cx.bar(B_KVH + s), 1);
     ptx::mbar_init(cx.bar(B_FIN), rank == 0 ? kQkIssuers : 1);
     misc[1] = 0;
     misc[3] = 0;
+    misc[4] = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -485,22 +481,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (rank == 0 || sparse) {
         // the segment's Q [128 heads][576] comes through the ring ahead of its
         // blocks, as fills of chunks 0-3, 4-7 and 8 (16 KB each); the issuers
-        // copy it into TMEM. With the shared ring (sparse) the fills land in
-        // both CTAs, rank 1 only accounts for their bytes.
+        // copy it into TMEM. With the shared ring (sparse) rank 0's Q counts as
+        // its own part (KVH), and rank 1 passes the same fills with an empty
+        // arrival on KVF: its KVH counts only the blocks it gathers, so that
+        // the forwarding warp, which skips Q fills, can never be two phases
+        // behind on a stage.
         for (int qb = 0; qb < 3 && ok; ++qb, ++m) {
           const int s = m % kNst;
           if (lane == 0) {
             ok = cx.wait(B_KVE + s, (uint32_t(m / kNst) & 1u) ^ 1u);
             if (ok) {
               const int nch = qb < 2 ? 4 : 1;
-              ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), uint32_t(nch) * kQChunkBytes);
-              for (int c = 0; c < nch && rank == 0; ++c) {
-                const uint32_t dst = cx.sbase + kOffRing + s * kMainBytes + c * kQChunkBytes;
-                if (sparse)
-                  tma3_mc(dst, &tq, cx.bar(B_KVF + s), 0, b * kHeads, 4 * qb + c, 0x3, pol);
-                else
-                  tma3(dst, &tq, cx.bar(B_KVF + s), 0, b * kHeads, 4 * qb + c, pol);
+              const uint32_t qbar = cx.bar((sparse ? B_KVH : B_KVF) + s);
+              if (rank == 0) {
+                ptx::mbar_arrive_expect_tx(qbar, uint32_t(nch) * kQChunkBytes);
+                for (int c = 0; c < nch; ++c)
+                  tma3(cx.sbase + kOffRing + s * kMainBytes + c * kQChunkBytes, &tq, qbar, 0, b * kHeads, 4 * qb + c,
+                       pol);
               }
+              if (sparse) ptx::mbar_arrive(cx.bar(B_KVF + s));  // nothing comes from the partner
               misc[3] = uint32_t(m + 1);
             }
           }
@@ -544,16 +543,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the block is list entries [w0, w0 + 64): tile::gather4 TMA copies
           // bring 4 listed cache rows x 64 columns per op into the 128-byte
           // swizzled stage (16 ops per column chunk, lane c issuing chunk c).
-          // The ring is shared: value chunks 0-3 come from rank 0 and 4-7 from
-          // rank 1, each multicast into both CTAs, and rank 0 alone loads the
-          // rope chunk, so each SM's TMA unit issues about half of the block.
+          // The ring is shared: rank 0 gathers value chunks 0-3 and the rope
+          // chunk, rank 1 chunks 4-7, each into its own stage (barrier KVH),
+          // and each CTA passes its value half to the partner's stage (the
+          // partner's KVF) with one 32 KB bulk copy, so each SM's TMA unit
+          // issues about half of the block's gather operations (plain ones:
+          // a multicast gather costs the issuing SM about twice as much).
           // Entries past the list read row 0 of the cache: their scores are
           // masked and rank 1 zeroes their V rows.
           if (lane == 0) {
             ok = (rank == 0 || g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
                  (rank == 1 || cx.wait(B_RE0 + (g & 1), uint32_t((g >> 1) & 1) ^ 1u));
-            if (ok)
-              ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), rank == 0 ? kMainBytes + kChunkBytes : kMainBytes);
+            if (ok) {
+              ptx::mbar_arrive_expect_tx(cx.bar(B_KVH + s), rank == 0 ? kMainBytes / 2 + kChunkBytes : kMainBytes / 2);
+              ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), kMainBytes / 2);
+              misc[4] = (misc[4] ^ (1u << s)) | (256u << s);
+            }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
@@ -569,13 +574,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int t = 4 * i + u;
               r4[u] = __shfl_sync(0xffffffffu, t < 32 ? ra : rb, t & 31);
             }
-            if (mine) {
-              if (lane < 8)
-                tma_gather4_mc(ring + lane * kChunkBytes + uint32_t(i) * 512, &tg, cx.bar(B_KVF + s), lane * 64, r4[0],
-                               r4[1], r4[2], r4[3], 0x3);
-              else
-                tma_gather4(rope + uint32_t(i) * 512, &tg, cx.bar(B_KVF + s), lane * 64, r4[0], r4[1], r4[2], r4[3]);
-            }
+            if (mine)
+              tma_gather4((lane < 8 ? ring + lane * kChunkBytes : rope) + uint32_t(i) * 512, &tg, cx.bar(B_KVH + s),
+                          lane * 64, r4[0], r4[1], r4[2], r4[3]);
           }
           if (lane == 0) misc[3] = uint32_t(m + 1);
           continue;
@@ -606,6 +607,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || (rank == 0 && warp >= 10)) {
     // ============================ MMA issuers ================================
     if (lane == 0) {
+      const uint32_t half_src = cx.sbase + kOffRing;  // rank 0's value half: chunks 0-3 of a stage
       int g = 0;
       bool ok = true;
       if (rank == 0) {
@@ -623,7 +625,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // from the ring into TMEM, once the score MMAs of the previous block
           // (the last readers of those columns) are complete
           if (g > 0) ok = cx.wait(B_SF0, uint32_t((g - 1) & 1));
-          for (int qb = 0; qb < 3 && ok; ++qb) ok = cx.wait(B_KVF + (m + qb) % kNst, uint32_t((m + qb) / kNst) & 1u);
+          for (int qb = 0; qb < 3 && ok; ++qb) {
+            const uint32_t par = uint32_t((m + qb) / kNst) & 1u;
+            ok = cx.wait_fill((m + qb) % kNst, par, sparse, par);
+          }
           if (!ok) break;
           tc_fence_after();
           if (g == 0 && qi == 0) arrive_remote(cx.peer_addr(cx.bar(B_Q0)));
@@ -643,7 +648,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m += 3;
           for (int j = 0; j < nb && ok; ++j, ++g, ++m) {
             const int s = m % kNst;
-            if (!cx.wait(B_KVF + s, uint32_t(m / kNst) & 1u) || !cx.wait(B_SE0, uint32_t(g & 1) ^ 1u)) {
+            if (sparse && qi == 0) {
+              // issuer 0 passes rank 0's gathered value half to rank 1 as soon
+              // as it has landed (it waits for this stage anyway)
+              if (!cx.wait(B_KVH + s, uint32_t(m / kNst) & 1u)) {
+                ok = false;
+                break;
+              }
+              const uint32_t src = half_src + uint32_t(s) * kMainBytes;
+              bulk_s2s(cx.peer_addr(src), src, kMainBytes / 2, cx.peer_addr(cx.bar(B_KVF + s)));
+              bulk_commit();
+            }
+            const uint32_t par = uint32_t(m / kNst) & 1u;
+            if (!cx.wait_fill(s, par, sparse, par) || !cx.wait(B_SE0, uint32_t(g & 1) ^ 1u)) {
               ok = false;
               break;
             }
@@ -659,6 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 umma_ts(dS, tmem + kTQ + c * 32 + kk * 8, sdesc(bc + kk * 32, 16, 1024), id_qk, (cc | kk) != 0);
             }
             umma_commit(cx.bar(B_SF0));
+            if (sparse && qi == 0) bulk_wait_read0();  // the copy to rank 1 has read the stage
             if (sparse)
               umma_commit_mc(cx.bar(B_KVE + s), 0x3);  // the stage is shared with rank 1
             else
@@ -669,6 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       } else {
         constexpr uint32_t id_pv = idesc(kHeads, 256, 1);
         int m = 0;  // ring fills: the blocks, and with the shared ring (sparse) rank 0's Q fills too
+        uint32_t hp = 0;  // per stage, parity of this CTA's next gather phase (KVH counts blocks only)
         for (int si = seg_lo; si < seg_hi && ok; ++si) {
           const int4 sg = segs[si];
           if (sg.z <= sg.y) continue;
@@ -682,10 +701,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           for (int j = 0; j < nb && ok; ++j, ++g, ++m) {
             const int s = m % kNst, pb = g & 1;
-            if (!cx.wait(B_KVF + s, uint32_t(m / kNst) & 1u) || !cx.wait(B_OR0 + pb, uint32_t((g >> 1) & 1))) {
+            if (!cx.wait_fill(s, uint32_t(m / kNst) & 1u, sparse, (hp >> s) & 1u) ||
+                !cx.wait(B_OR0 + pb, uint32_t((g >> 1) & 1))) {
               ok = false;
               break;
             }
+            hp ^= 1u << s;
             tc_fence_after();
             const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
             const uint32_t pbuf = cx.sbase + kOffP + pb * kPBytes;
@@ -705,6 +726,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (sparse) bulk_wait0();  // rank 0 issuer 0's copies to rank 1 have read their stages
       // every MMA this thread issued has completed before TMEM is released
       umma_commit(cx.bar(B_FIN));
       ptx::mbar_wait(cx.bar(B_FIN), 0, nullptr, kWaitCycles);
@@ -854,6 +876,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tOh = tmem + kTO + lane_off + 256 * hc;  // this thread's row, this half's columns
     const int col0 = 256 * hc;
     int g = 0, m = 0, stn = 0;  // blocks, ring fills (the shared ring also carries Q fills)
+    uint32_t hp = 0;            // per stage, parity of this CTA's next gather phase (sparse)
     bool ok = true;
     for (int si = seg_lo; si < seg_hi; ++si) {
       const int4 sg = segs[si];
@@ -899,7 +922,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // every consumer, so that the parity test below can only be passed
           // by this block's fill)
           if (sparse && m >= kNst) ok = ok && cx.wait(B_KVE + s, uint32_t((m - kNst) / kNst) & 1u);
-          ok = ok && cx.wait(B_KVF + s, uint32_t(m / kNst) & 1u);
+          ok = ok && cx.wait_fill(s, uint32_t(m / kNst) & 1u, sparse, (hp >> s) & 1u);
           const int t_lo = max(0, min(kBlk, L - w0));
           const int nrow = kBlk - t_lo;
           uint8_t *stg = smem + kOffRing + uint32_t(s) * kMainBytes;
@@ -911,6 +934,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           ptx::fence_proxy_async_smem();  // zeros are read by the tensor core (async proxy)
         }
+        hp ^= 1u << s;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(cx.bar(B_OR0 + pb));
@@ -1177,6 +1201,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();  // O reads done before the next segment's first PV overwrites it
     }
     (void)ok;
+  } else if (sparse && rank == 1 && warp == 10) {
+    // ======== sparse, rank 1: pass the gathered value half (chunks 4-7) to rank 0 ========
+    // (one 32 KB bulk copy per block into rank 0's stage, counted on its KVF, as
+    // soon as it landed here: rank 0 needs it before P, and so before rank 1's PV).
+    // This warp releases every fill of the ring here, the copied ones once the
+    // copy has read them, so no barrier it waits on can run two phases ahead.
+    if (lane == 0) {
+      int m = 0;
+      uint32_t hp = 0;  // per stage, parity of the next gather phase (KVH counts blocks only)
+      bool ok = true;
+      for (int si = seg_lo; si < seg_hi && ok; ++si) {
+        const int4 sg = segs[si];
+        if (sg.z <= sg.y) continue;
+        const int nb = num_blocks(sg.y, sg.z);
+        // the segment's Q fills carry nothing for rank 0: release each once the
+        // stage's previous fill is released (the phase this arrival belongs to
+        // has then begun; a wait on KVF could pass on the previous block's phase)
+        for (int qb = 0; qb < 3 && ok; ++qb, ++m) {
+          ok = cx.wait(B_KVE + m % kNst, (uint32_t(m / kNst) & 1u) ^ 1u);
+          if (ok) ptx::mbar_arrive(cx.bar(B_KVE + m % kNst));
+        }
+        for (int j = 0; j < nb && ok; ++j, ++m) {
+          const int s = m % kNst;
+          ok = cx.wait(B_KVH + s, (hp >> s) & 1u);
+          if (!ok) break;
+          hp ^= 1u << s;
+          const uint32_t src = cx.sbase + kOffRing + uint32_t(s) * kMainBytes + kMainBytes / 2;
+          bulk_s2s(cx.peer_addr(src), src, kMainBytes / 2, cx.peer_addr(cx.bar(B_KVF + s)));
+          bulk_commit();
+          bulk_wait_read0();
+          ptx::mbar_arrive(cx.bar(B_KVE + s));
+        }
+      }
+      bulk_wait0();  // the copies are complete before the CTAs leave
+    }
   }
   // ---- teardown: both ranks leave together (the partner may still write here) ----
   tc_fence_before();
@@ -1185,8 +1244,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *cx.abort) {
     // after a give-up, wait (bounded) for the copies still in flight into this CTA
     const int n = int(misc[3]);
-    for (int i = max(0, n - kNst); i < n; ++i)
+    for (int i = max(0, n - kNst); i < n; ++i) {
       ptx::mbar_wait(cx.bar(B_KVF + i % kNst), uint32_t(i / kNst) & 1u, nullptr, kWaitCycles);
+      if (sparse && rank == 0) ptx::mbar_wait(cx.bar(B_KVH + i % kNst), uint32_t(i / kNst) & 1u, nullptr, kWaitCycles);
+    }
+    // rank 1's KVH counts its gather phases only: wait for the last one of each stage
+    const uint32_t hm = misc[4];
+    for (int st = 0; st < kNst && sparse && rank == 1; ++st)
+      if ((hm >> (8 + st)) & 1u) ptx::mbar_wait(cx.bar(B_KVH + st), ((hm >> st) & 1u) ^ 1u, nullptr, kWaitCycles);
   }
   __syncthreads();
   if (warp == 1) {
@@ -1207,8 +1272,10 @@ namespace {
 int set_smem_attr() {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
+            cudaSuccess)
       return SKD_ECUDA;
     attr_set = true;
   }
@@ -1224,7 +1291,7 @@ int mla_resident_workers(int *n) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   int v = 0;
-  if (cudaOccupancyMaxActiveClusters(&v, mla_decode_kernel, &cfg) != cudaSuccess) return SKD_ECUDA;
+  if (cudaOccupancyMaxActiveClusters(&v, mla_decode_kernel<false>, &cfg) != cudaSuccess) return SKD_ECUDA;
   *n = v;
   return SKD_OK;
 }
@@ -1312,7 +1379,8 @@ int launch_mla(const DecodeArgs &a) {
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, tmain, trope, tpart, tout, tq, tg, p) != cudaSuccess) return SKD_ECUDA;
+  auto kern = p.topk ? mla_decode_kernel<true> : mla_decode_kernel<false>;
+  if (cudaLaunchKernelEx(&cfg, kern, tmain, trope, tpart, tout, tq, tg, p) != cudaSuccess) return SKD_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 
