@@ -51,6 +51,8 @@ def _args():
                     help="fixed_split = the two-kernel split-KV comparator (fixed splits + combine kernel)")
     ap.add_argument("--seg-cost", type=int, default=None,
                     help="planner's per-segment cost in granules (default: the library's per-kind default)")
+    ap.add_argument("--align", type=int, default=None,
+                    help="planner's cut unit in granules (default: the library's per-kind default)")
     ap.add_argument("--n-ctas", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample (cpu_baseline)")
@@ -91,20 +93,20 @@ def _measured_hbm_peak():
     return (v, "measured (MEASURED_PEAKS.json hbm_gbs)") if v else (FALLBACK_HBM_GBS, "fallback")
 
 
-def _launch_study(skd, q, k, v, pt, sl, w, shape, n, seg_cost, ws, out, lse, a):
+def _launch_study(skd, q, k, v, pt, sl, w, shape, n, seg_cost, align, ws, out, lse, a):
     """Per-step time of device planner + attention, four ways: eager launches or
     one CUDA graph replay, each with programmatic dependent launch on or off.
     The difference to the kernel time alone is what launching costs per step."""
     import torch
     hkv = shape.num_kv_heads
-    plan = skd.plan_device(sl, hkv, w.page_size, n, seg_cost=seg_cost)
+    plan = skd.plan_device(sl, hkv, w.page_size, n, seg_cost=seg_cost, align=align)
     res = {}
     steps = max(50, min(a.steps, 500))
     for pdl in (False, True):
         skd.set_pdl(pdl)
 
         def step():
-            skd.plan_device(sl, hkv, w.page_size, n, out=plan, seg_cost=seg_cost)
+            skd.plan_device(sl, hkv, w.page_size, n, out=plan, seg_cost=seg_cost, align=align)
             skd.decode_attention(q, k, v, pt, sl, plan, ws, scale=w.scale, causal=w.causal, n_ctas=n,
                                  out=out, lse=lse, shape=shape)
 
@@ -313,7 +315,8 @@ def run_ours(a):
     n = a.n_ctas or skd.default_ctas(shape)
     seg_cost = 0 if a.mode != "streamk" else (skd.default_seg_cost(shape, sparse=sparse) if a.seg_cost is None
                                               else a.seg_cost)
-    plan_h = skd.plan(plan_lens, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)
+    align = 1 if a.mode != "streamk" else (skd.default_align(shape) if a.align is None else a.align)
+    plan_h = skd.plan(plan_lens, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost, align=align)
     plan_d = plan_h.to(dev)
     ws = skd.workspace(shape, n, dev)
     out = torch.empty(w.batch, w.q_tokens, w.num_q_heads, w.head_dim_v, dtype=torch.bfloat16, device=dev)
@@ -389,7 +392,7 @@ def run_ours(a):
     err = skd.read_error(ws)
     if err != 0:
         raise RuntimeError(f"device error word {err}")
-    launch = _launch_study(skd, q, k, v, pt, sl, w, shape, n, seg_cost, ws, out, lse, a) if a.launch_study else None
+    launch = _launch_study(skd, q, k, v, pt, sl, w, shape, n, seg_cost, align, ws, out, lse, a) if a.launch_study else None
     if prefix is not None:
         for wsx in prefix.workspaces():
             if skd.read_error(wsx) != 0:
@@ -439,7 +442,8 @@ def run_ours(a):
 
         def e2e_step():
             lens_h = tl_h if sparse else sl_h
-            p = skd.plan(lens_h, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost)  # host planner
+            p = skd.plan(lens_h, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost,
+                         align=align)  # host planner
             plan_pin.copy_(p)
             q_d.copy_(q_h, non_blocking=True)
             pt_d.copy_(pt_h, non_blocking=True)
@@ -496,7 +500,7 @@ def run_ours(a):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
         "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "workload"},
-                   "n_ctas": n, "plan": a.mode, "seg_cost": seg_cost, "algorithmic_bytes": alg_bytes,
+                   "n_ctas": n, "plan": a.mode, "seg_cost": seg_cost, "align": align, "algorithmic_bytes": alg_bytes,
                    "l2": ("flushed before each timed step (256 MB write, outside the step's events)"
                           if flush is not None else "no flush: KV per step is larger than L2 (129 MB)"),
                    "parallelism": f"replicas x{world}"},

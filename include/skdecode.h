@@ -170,6 +170,23 @@ int skd_decode_plan_weighted_device(const int32_t *seqlens_dev, int batch, int n
                                     int n_ctas, int seg_cost, void *plan_dev, size_t plan_bytes,
                                     void *stream);
 
+/* Weighted split with aligned split points (a second extension). The equal
+ * split runs over cut units of `align` granules instead of single granules:
+ * work item i has ceil(seqlens[b] / (SKD_GRANULE * align)) units, preceded
+ * (when non-empty) by ceil(seg_cost / align) virtual units, and every split
+ * point inside an item falls on a multiple of SKD_GRANULE * align tokens. A
+ * kernel that reads an item in whole blocks of that many tokens (the MLA
+ * kernel: 64 tokens, align = 4) then never reads one block in two splits.
+ * align = 1 gives exactly skd_decode_plan_weighted's plan. 1 <= align <= 64,
+ * else SKD_EINVAL; other arguments and errors as skd_decode_plan_weighted /
+ * skd_decode_plan_weighted_device. Host and device variants produce identical
+ * bytes; align is stored in the plan header. */
+int skd_decode_plan_aligned(const int32_t *seqlens_host, int batch, int num_kv_heads, int page_size,
+                            int n_ctas, int seg_cost, int align, void *plan_host, size_t plan_bytes);
+int skd_decode_plan_aligned_device(const int32_t *seqlens_dev, int batch, int num_kv_heads, int page_size,
+                                   int n_ctas, int seg_cost, int align, void *plan_dev, size_t plan_bytes,
+                                   void *stream);
+
 /* The two-kernel split-KV comparator (the design the pages measure MeldKernel
  * against: split-KV with fixed splits and a separate combine pass). Same
  * arguments as skd_decode_attention; plan_dev should come from skd_decode_plan

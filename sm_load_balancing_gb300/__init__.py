@@ -23,7 +23,7 @@ from ._native import (SKD_DEVERR_INDEX, SKD_DEVERR_PAGE, SKD_DEVERR_PLAN, SKD_DE
                       SKD_DEVERR_TIMEOUT, SKD_GRANULE, SkdError)
 
 __all__ = ["plan", "plan_device", "plan_bytes", "workspace", "decode_attention", "decode_attention_sparse",
-           "read_error", "sm_count", "default_ctas", "default_seg_cost", "make_shape", "set_pdl", "SkdError",
+           "read_error", "sm_count", "default_ctas", "default_seg_cost", "default_align", "make_shape", "set_pdl", "SkdError",
            "SKD_GRANULE", "SKD_DEVERR_PLAN", "SKD_DEVERR_SEQLEN", "SKD_DEVERR_PAGE", "SKD_DEVERR_TIMEOUT",
            "SKD_DEVERR_INDEX"]
 
@@ -59,10 +59,10 @@ def default_ctas(shape: Optional[N.Shape] = None, device: Optional[int] = None) 
 # loading a request's 128 query rows into TMEM and draining its 128x512
 # accumulator cost a few microseconds, which the dense kernel streams as
 # roughly this many granules. The sparse (top-k) path gathers its rows and
-# spends about five times as long per granule, so the same cost is fewer
+# spends several times as long per granule, so the same cost is fewer
 # granules there.
 MLA_SEG_COST = 40
-MLA_SPARSE_SEG_COST = 8
+MLA_SPARSE_SEG_COST = 4
 
 
 def default_seg_cost(shape: Optional[N.Shape] = None, sparse: bool = False) -> int:
@@ -74,16 +74,31 @@ def default_seg_cost(shape: Optional[N.Shape] = None, sparse: bool = False) -> i
     return MLA_SPARSE_SEG_COST if sparse else MLA_SEG_COST
 
 
+# The absorbed-MLA kernel reads a request in whole blocks of 64 tokens (4
+# granules): plans for it cut only at block boundaries, so no block is read by
+# two splits.
+MLA_ALIGN = 4
+
+
+def default_align(shape: Optional[N.Shape] = None) -> int:
+    """Granules per cut unit the planner uses by default: the MLA kernel's
+    64-token block, 1 (any granule) for the GQA kernel."""
+    if shape is None or shape.kind != N.SKD_KIND_MLA:
+        return 1
+    return MLA_ALIGN
+
+
 def plan_bytes(batch: int, num_kv_heads: int, n_ctas: int) -> int:
     return int(N.lib().skd_plan_bytes(batch, num_kv_heads, n_ctas))
 
 
 def plan(seqlens, num_kv_heads: int, page_size: int, n_ctas: Optional[int] = None,
-         mode: str = "streamk", seg_cost: int = 0) -> torch.Tensor:
+         mode: str = "streamk", seg_cost: int = 0, align: int = 1) -> torch.Tensor:
     """Host planner. ``seqlens``: CPU int32 tensor (or anything torch.as_tensor
-    takes). ``seg_cost``: virtual granules charged per work item (Stream-K
-    only; 0 = the plain equal split). Returns the plan as a CPU int32 tensor;
-    copy it to the device."""
+    takes). ``seg_cost``: virtual granules charged per work item; ``align``:
+    split points on multiples of 16 * align tokens (both Stream-K only; 0 and
+    1 = the plain equal split). Returns the plan as a CPU int32 tensor; copy it
+    to the device."""
     sl = torch.as_tensor(seqlens, dtype=torch.int32).contiguous()
     if sl.device.type != "cpu":
         raise ValueError("plan() takes host seqlens; use plan_device() for device seqlens")
@@ -93,12 +108,12 @@ def plan(seqlens, num_kv_heads: int, page_size: int, n_ctas: Optional[int] = Non
         raise ValueError("invalid batch / num_kv_heads / n_ctas")
     out = torch.zeros(nb // 4, dtype=torch.int32)
     if mode == "streamk":
-        N.check("skd_decode_plan_weighted", N.lib().skd_decode_plan_weighted(
-            sl.data_ptr(), int(sl.numel()), int(num_kv_heads), int(page_size), n, int(seg_cost),
+        N.check("skd_decode_plan_aligned", N.lib().skd_decode_plan_aligned(
+            sl.data_ptr(), int(sl.numel()), int(num_kv_heads), int(page_size), n, int(seg_cost), int(align),
             out.data_ptr(), nb))
     else:
-        if seg_cost:
-            raise ValueError("seg_cost applies to the streamk mode only")
+        if seg_cost or align != 1:
+            raise ValueError("seg_cost and align apply to the streamk mode only")
         N.check("skd_decode_plan", N.lib().skd_decode_plan(
             sl.data_ptr(), int(sl.numel()), int(num_kv_heads), int(page_size), n, _MODES[mode],
             out.data_ptr(), nb))
@@ -107,7 +122,7 @@ def plan(seqlens, num_kv_heads: int, page_size: int, n_ctas: Optional[int] = Non
 
 def plan_device(seqlens: torch.Tensor, num_kv_heads: int, page_size: int, n_ctas: int,
                 out: Optional[torch.Tensor] = None,
-                stream: Optional[torch.cuda.Stream] = None, seg_cost: int = 0) -> torch.Tensor:
+                stream: Optional[torch.cuda.Stream] = None, seg_cost: int = 0, align: int = 1) -> torch.Tensor:
     """Device planner (graph capturable), byte-identical to ``plan``.
     ``seqlens``: CUDA int32 tensor."""
     if seqlens.device.type != "cuda" or seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
@@ -115,9 +130,9 @@ def plan_device(seqlens: torch.Tensor, num_kv_heads: int, page_size: int, n_ctas
     nb = plan_bytes(int(seqlens.numel()), num_kv_heads, n_ctas)
     if out is None:
         out = torch.empty(nb // 4, dtype=torch.int32, device=seqlens.device)
-    N.check("skd_decode_plan_weighted_device", N.lib().skd_decode_plan_weighted_device(
+    N.check("skd_decode_plan_aligned_device", N.lib().skd_decode_plan_aligned_device(
         seqlens.data_ptr(), int(seqlens.numel()), int(num_kv_heads), int(page_size), int(n_ctas),
-        int(seg_cost), out.data_ptr(), out.numel() * 4, _stream_ptr(stream)))
+        int(seg_cost), int(align), out.data_ptr(), out.numel() * 4, _stream_ptr(stream)))
     return out
 
 

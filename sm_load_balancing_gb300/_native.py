@@ -41,6 +41,9 @@ SIGNATURES = {
     "skd_decode_plan_device": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
     "skd_decode_plan_weighted": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size]),
     "skd_decode_plan_weighted_device": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
+    "skd_decode_plan_aligned": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size]),
+    "skd_decode_plan_aligned_device": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size,
+                                                 _vp]),
     "skd_workspace_bytes": (_c_size, [ctypes.POINTER(Shape), _c_int]),
     "skd_workspace_reset": (_c_int, [_vp, _c_size, _vp]),
     "skd_decode_attention": (_c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _c_int,

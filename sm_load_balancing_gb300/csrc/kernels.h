@@ -50,7 +50,7 @@ int launch_gather_rows(void *dst, const void *src, const int32_t *src_rows, int6
 int launch_merge_states(const void *out_a, const float *lse_a, const int32_t *a_rows, const void *out_b,
                         const float *lse_b, const int32_t *b_rows, void *out, float *lse, int64_t n_rows,
                         int head_dim_v, cudaStream_t stream);
-int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n_ctas, int seg_cost, int32_t *plan,
+int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n_ctas, int seg_cost, int align, int32_t *plan,
                        cudaStream_t stream);
 
 // cuTensorMapEncodeTiled, looked up through the runtime (no libcuda link).

@@ -87,16 +87,18 @@ __device__ int block_exclusive_scan(int32_t *a, int len, int32_t *warp_sums, int
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
-    plan_device_kernel(const int32_t *__restrict__ seqlens, int batch, int ngrp, int n, int seg_cost,
+    plan_device_kernel(const int32_t *__restrict__ seqlens, int batch, int ngrp, int n, int seg_cost, int align,
                        int32_t *__restrict__ plan) {
   extern __shared__ int32_t sm[];
-  int32_t *req_pref = sm;                 // [batch + 1] virtual-granule prefix per request
+  int32_t *req_pref = sm;                 // [batch + 1] virtual-unit prefix per request
   int32_t *cnt = req_pref + batch + 1;    // [n + 1] segments per CTA -> offsets
   int32_t *first = cnt + n + 1;           // [n] smallest item of each CTA
   __shared__ int32_t warp_sums[33];
   __shared__ int32_t carry;
   __shared__ int32_t err;
   const int tid = threadIdx.x;
+  const int unit = kGranule * align;                 // tokens per cut unit
+  const int vcost = (seg_cost + align - 1) / align;  // virtual units per item
   // the attention kernel that follows may be scheduled now: it waits for this
   // grid to complete (griddepcontrol.wait) before reading the plan
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -111,8 +113,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   for (int b = tid; b < batch; b += kPlanThreads) {
     const int L = seqlens[b];
     if (L < 0) atomicOr(&err, SKD_DEVERR_SEQLEN);
-    // each of the request's ngrp items: its segment cost, then its granules
-    req_pref[b] = L > 0 ? (L + kGranule - 1) / kGranule + seg_cost : 0;
+    // each of the request's ngrp items: its segment cost, then its units
+    req_pref[b] = L > 0 ? (L + unit - 1) / unit + vcost : 0;
   }
   for (int c = tid; c <= n; c += kPlanThreads) cnt[c] = 0;
   for (int c = tid; c < n; c += kPlanThreads) first[c] = 0x7fffffff;
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   for (int64_t i = tid; i < items; i += kPlanThreads) {
     const int b = int(i / ngrp), h = int(i - int64_t(b) * ngrp);
     const int64_t gv = req_pref[b + 1] - req_pref[b];  // virtual length of each item of b
-    const int64_t g = gv > 0 ? gv - seg_cost : 0;
+    const int64_t g = gv > 0 ? gv - vcost : 0;
     const int64_t s = int64_t(ngrp) * req_pref[b] + h * gv + (gv - g), e = s + g;
     int ns = 0;
     if (g == 0) {
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     const int b = int(i / ngrp), h = int(i - int64_t(b) * ngrp);
     const int L = seqlens[b];
     const int64_t gv = req_pref[b + 1] - req_pref[b];
-    const int64_t g = gv > 0 ? gv - seg_cost : 0;
+    const int64_t g = gv > 0 ? gv - vcost : 0;
     const int64_t s = int64_t(ngrp) * req_pref[b] + h * gv + (gv - g), e = s + g;
     const int ns = nsplit[i];
     const int sl0 = ns > 1 ? slot0[i] : -1;
@@ -192,8 +194,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
         const int64_t lo_c = bw.lo, hi_c = bw.hi;
         if (hi_c <= lo_c) continue;
         const int64_t lo = s > lo_c ? s : lo_c, hi = e < hi_c ? e : hi_c;
-        const int64_t tb = (lo - s) * kGranule;
-        const int64_t te = (hi - s) * kGranule < L ? (hi - s) * kGranule : L;
+        const int64_t tb = (lo - s) * unit;
+        const int64_t te = (hi - s) * unit < L ? (hi - s) * unit : L;
         segs[cnt[c] + (i - first[c])] = make_int4(int(i), int(tb), int(te), ns > 1 ? sl0 + k : -1);
         ++k;
       }
@@ -220,21 +222,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     plan[PH_SEGCAP] = int(cap);
     plan[PH_ERR] = 0;
     plan[PH_SEGCOST] = seg_cost;
+    plan[PH_ALIGN] = align;
   }
 }
 
 }  // namespace
 
-int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n, int seg_cost, int32_t *plan,
+int launch_plan_device(const int32_t *seqlens, int batch, int ngrp, int n, int seg_cost, int align, int32_t *plan,
                        cudaStream_t stream) {
-  if (seg_cost < 0 || seg_cost > kMaxSegCost) return SKD_EINVAL;
+  if (seg_cost < 0 || seg_cost > kMaxSegCost || align < 1 || align > kMaxAlign) return SKD_EINVAL;
   const size_t smem = size_t(batch + 1 + 2 * (n + 1)) * 4;
   if (smem > 200 * 1024) return SKD_EUNSUPPORTED;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(plan_device_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return SKD_ECUDA;
-  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seqlens, batch, ngrp, n, seg_cost, plan);
+  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seqlens, batch, ngrp, n, seg_cost, align, plan);
   return cudaGetLastError() == cudaSuccess ? SKD_OK : SKD_ECUDA;
 }
 

@@ -16,6 +16,12 @@
 // its output or partial state). The equal split then runs over the virtual
 // total, so a CTA that crosses many item boundaries receives fewer tokens.
 // seg_cost = 0 is the plain split.
+//
+// Optional alignment (also an extension): with align > 1 the split runs over
+// cut units of align granules, so split points fall on multiples of
+// kGranule * align tokens of an item (a kernel that reads whole blocks of that
+// many tokens then never reads a block twice), and the segment cost is
+// ceil(seg_cost / align) units. align = 1 is the plan above.
 #include <string.h>
 
 #include <vector>
@@ -28,12 +34,15 @@ namespace skd {
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, int n, int mode,
-                    int seg_cost, void *plan_out, size_t plan_bytes) {
+                    int seg_cost, int align, void *plan_out, size_t plan_bytes) {
   if (!seqlens && batch > 0) return SKD_EINVAL;
   if (!plan_out || batch < 0 || ngrp <= 0 || n <= 0) return SKD_EINVAL;
   if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
   if (mode != SKD_PLAN_STREAMK && mode != SKD_PLAN_ROUND_ROBIN && mode != SKD_PLAN_FIXED_SPLIT) return SKD_EINVAL;
   if (seg_cost < 0 || seg_cost > kMaxSegCost || (seg_cost > 0 && mode != SKD_PLAN_STREAMK)) return SKD_EINVAL;
+  if (align < 1 || align > kMaxAlign || (align > 1 && mode != SKD_PLAN_STREAMK)) return SKD_EINVAL;
+  const int64_t unit = int64_t(kGranule) * align;                // tokens per cut unit
+  const int64_t vcost = ceil_div(seg_cost, align);               // virtual units per item
   const PlanOffsets off = plan_offsets(batch, ngrp, n);
   if (plan_bytes < size_t(off.words) * 4) return SKD_EPLAN;
   for (int b = 0; b < batch; ++b)
@@ -48,10 +57,10 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
   int32_t *nsplit = w + off.nsplit;
   int32_t *slot0 = w + off.slot0;
 
-  int64_t total = 0;  // virtual granules
+  int64_t total = 0;  // virtual cut units (granules when align = 1)
   for (int b = 0; b < batch; ++b) {
-    const int64_t g = ceil_div(seqlens[b], kGranule);
-    total += int64_t(ngrp) * (g + (g > 0 ? seg_cost : 0));
+    const int64_t g = ceil_div(seqlens[b], unit);
+    total += int64_t(ngrp) * (g + (g > 0 ? vcost : 0));
   }
   if (total > INT32_MAX) return SKD_EPLAN;
 
@@ -78,9 +87,9 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
     };
     for (int64_t i = 0; i < items; ++i) {
       const int64_t L = seqlens[i / ngrp];
-      const int64_t g = ceil_div(L, kGranule);
-      // token granules of the item occupy [s, e) after its virtual segment cost
-      const int64_t s = pos + (g > 0 ? seg_cost : 0), e = s + g;
+      const int64_t g = ceil_div(L, unit);
+      // token units of the item occupy [s, e) after its virtual segment cost
+      const int64_t s = pos + (g > 0 ? vcost : 0), e = s + g;
       pos = e;
       // first CTA whose chunk ends after s (the last CTA if none)
       int64_t cs = c;
@@ -98,8 +107,8 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
           continue;
         }
         close_ctas_up_to(cc);
-        const int64_t tb = (lo - s) * kGranule;
-        const int64_t te = (hi - s) * kGranule < L ? (hi - s) * kGranule : L;
+        const int64_t tb = (lo - s) * unit;
+        const int64_t te = (hi - s) * unit < L ? (hi - s) * unit : L;
         push(i, tb, te);
       }
     }
@@ -178,6 +187,7 @@ int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, 
   w[PH_SEGCAP] = int32_t(cap);
   w[PH_ERR] = 0;
   w[PH_SEGCOST] = seg_cost;
+  w[PH_ALIGN] = align;
   return SKD_OK;
 }
 

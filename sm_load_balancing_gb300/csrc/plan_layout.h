@@ -30,6 +30,7 @@ SKD_HD inline int head_group(int hkv) {
 constexpr int32_t kPlanMagic = 0x534B4431;  // "SKD1"
 constexpr int kGranule = 16;
 constexpr int kMaxSegCost = 1 << 16;  // granules
+constexpr int kMaxAlign = 64;         // granules per cut unit
 
 enum PlanHeader : int {
   PH_MAGIC = 0,
@@ -40,11 +41,12 @@ enum PlanHeader : int {
   PH_NITEMS = 5,
   PH_NSEGS = 6,
   PH_NSLOTS = 7,
-  PH_TOTAL = 8,  // total granules
+  PH_TOTAL = 8,  // total cut units (granules x PH_ALIGN)
   PH_MODE = 9,
   PH_SEGCAP = 10,
   PH_ERR = 11,  // device planner's error bits (SKD_DEVERR_*), 0 from the host planner
   PH_SEGCOST = 12,  // virtual granules charged per non-empty item (0: plain split)
+  PH_ALIGN = 13,    // granules per cut unit: split points fall on multiples of kGranule * PH_ALIGN tokens
   PH_WORDS = 16
 };
 

@@ -13,7 +13,7 @@
 
 namespace skd {
 int build_plan_host(const int32_t *seqlens, int batch, int ngrp, int page_size, int n, int mode, int seg_cost,
-                    void *plan_out, size_t plan_bytes);
+                    int align, void *plan_out, size_t plan_bytes);
 
 namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -155,27 +155,40 @@ int skd_decode_plan(const int32_t *seqlens_host, int batch, int num_kv_heads, in
                     int n_ctas, int mode, void *plan_host, size_t plan_bytes) {
   if (num_kv_heads < 1) return SKD_EINVAL;
   return build_plan_host(seqlens_host, batch, num_kv_heads / head_group(num_kv_heads), page_size,
-                         n_ctas, mode, 0, plan_host, plan_bytes);
+                         n_ctas, mode, 0, 1, plan_host, plan_bytes);
+}
+
+int skd_decode_plan_aligned(const int32_t *seqlens_host, int batch, int num_kv_heads, int page_size,
+                            int n_ctas, int seg_cost, int align, void *plan_host, size_t plan_bytes) {
+  if (num_kv_heads < 1) return SKD_EINVAL;
+  return build_plan_host(seqlens_host, batch, num_kv_heads / head_group(num_kv_heads), page_size,
+                         n_ctas, SKD_PLAN_STREAMK, seg_cost, align, plan_host, plan_bytes);
 }
 
 int skd_decode_plan_weighted(const int32_t *seqlens_host, int batch, int num_kv_heads, int page_size,
                              int n_ctas, int seg_cost, void *plan_host, size_t plan_bytes) {
-  if (num_kv_heads < 1) return SKD_EINVAL;
-  return build_plan_host(seqlens_host, batch, num_kv_heads / head_group(num_kv_heads), page_size,
-                         n_ctas, SKD_PLAN_STREAMK, seg_cost, plan_host, plan_bytes);
+  return skd_decode_plan_aligned(seqlens_host, batch, num_kv_heads, page_size, n_ctas, seg_cost, 1, plan_host,
+                                 plan_bytes);
+}
+
+int skd_decode_plan_aligned_device(const int32_t *seqlens_dev, int batch, int num_kv_heads, int page_size,
+                                   int n_ctas, int seg_cost, int align, void *plan_dev, size_t plan_bytes,
+                                   void *stream) {
+  if ((!seqlens_dev && batch > 0) || !plan_dev || batch < 0 || num_kv_heads < 1 || n_ctas < 1)
+    return SKD_EINVAL;
+  if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
+  if (seg_cost < 0 || seg_cost > kMaxSegCost || align < 1 || align > kMaxAlign) return SKD_EINVAL;
+  if (!aligned(plan_dev, 16)) return SKD_EINVAL;
+  if (plan_bytes < skd_plan_bytes(batch, num_kv_heads, n_ctas)) return SKD_EPLAN;
+  return launch_plan_device(seqlens_dev, batch, num_kv_heads / head_group(num_kv_heads), n_ctas, seg_cost, align,
+                            static_cast<int32_t *>(plan_dev), static_cast<cudaStream_t>(stream));
 }
 
 int skd_decode_plan_weighted_device(const int32_t *seqlens_dev, int batch, int num_kv_heads, int page_size,
                                     int n_ctas, int seg_cost, void *plan_dev, size_t plan_bytes,
                                     void *stream) {
-  if ((!seqlens_dev && batch > 0) || !plan_dev || batch < 0 || num_kv_heads < 1 || n_ctas < 1)
-    return SKD_EINVAL;
-  if (page_size <= 0 || page_size % kGranule != 0) return SKD_EINVAL;
-  if (seg_cost < 0 || seg_cost > kMaxSegCost) return SKD_EINVAL;
-  if (!aligned(plan_dev, 16)) return SKD_EINVAL;
-  if (plan_bytes < skd_plan_bytes(batch, num_kv_heads, n_ctas)) return SKD_EPLAN;
-  return launch_plan_device(seqlens_dev, batch, num_kv_heads / head_group(num_kv_heads), n_ctas, seg_cost,
-                            static_cast<int32_t *>(plan_dev), static_cast<cudaStream_t>(stream));
+  return skd_decode_plan_aligned_device(seqlens_dev, batch, num_kv_heads, page_size, n_ctas, seg_cost, 1,
+                                        plan_dev, plan_bytes, stream);
 }
 
 int skd_decode_plan_device(const int32_t *seqlens_dev, int batch, int num_kv_heads, int page_size,

@@ -29,14 +29,16 @@ class Dev:
         self.shape = skd.make_shape(self.q, self.k, self.v, self.pt, scale=w.scale, causal=w.causal)
 
     def run(self, n_ctas=None, mode="streamk", plan=None, ws=None, out=None, lse=None, seg_cost=None,
-            two_kernel=False):
+            two_kernel=False, align=None):
         skd = self.skd
         n = skd.default_ctas(self.shape) if n_ctas is None else n_ctas
         if plan is None:
             if seg_cost is None:
                 seg_cost = skd.default_seg_cost(self.shape) if mode == "streamk" else 0
+            if align is None:
+                align = skd.default_align(self.shape) if mode == "streamk" else 1
             plan = skd.plan(self.w.seqlens, self.shape.num_kv_heads, self.w.page_size, n, mode,
-                            seg_cost=seg_cost).cuda()
+                            seg_cost=seg_cost, align=align).cuda()
         if ws is None:
             ws = skd.workspace(self.shape, n)
         o, l = skd.decode_attention(self.q, self.k, self.v, self.pt, self.sl, plan, ws,

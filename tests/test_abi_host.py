@@ -46,11 +46,14 @@ def test_every_declared_symbol_is_exported(N):
     assert lib.skd_abi_version() == 1
 
 
-def _host_plan(N, seqlens, hkv, n, mode=0, page_size=16, seg_cost=None):
+def _host_plan(N, seqlens, hkv, n, mode=0, page_size=16, seg_cost=None, align=None):
     sl = np.ascontiguousarray(seqlens, dtype=np.int32)
     nb = N.lib().skd_plan_bytes(len(sl), hkv, n)
     buf = np.zeros(nb // 4, dtype=np.int32)
-    if seg_cost is None:
+    if align is not None:
+        st = N.lib().skd_decode_plan_aligned(sl.ctypes.data, len(sl), hkv, page_size, n, seg_cost or 0, align,
+                                             buf.ctypes.data, nb)
+    elif seg_cost is None:
         st = N.lib().skd_decode_plan(sl.ctypes.data, len(sl), hkv, page_size, n, mode, buf.ctypes.data, nb)
     else:
         st = N.lib().skd_decode_plan_weighted(sl.ctypes.data, len(sl), hkv, page_size, n, seg_cost,
@@ -65,11 +68,15 @@ def head_groups(hkv):
     return hkv // hg
 
 
-def _check_against_oracle(N, seqlens, hkv, n, seg_cost=None):
-    st, buf = _host_plan(N, seqlens, hkv, n, seg_cost=seg_cost)
+def _check_against_oracle(N, seqlens, hkv, n, seg_cost=None, align=None):
+    st, buf = _host_plan(N, seqlens, hkv, n, seg_cost=seg_cost, align=align)
     assert st == 0
     p = PD.decode(buf)
-    ref = S.streamk_split(seqlens, head_groups(hkv), n, granule=16, seg_cost=seg_cost or 0)
+    # an aligned plan is the split over cut units of 16 * align tokens, each
+    # item's fixed cost rounded up to whole units
+    a = align or 1
+    ref = S.streamk_split(seqlens, head_groups(hkv), n, granule=16 * a, seg_cost=-(-(seg_cost or 0) // a))
+    assert buf[13] == a  # the header records the cut unit
     got = [[(i, tb, te) for i, tb, te, _ in segs] for segs in p["segments"]]
     assert got == ref["segments"]
     assert p["total"] == ref["total_granules"]
@@ -159,6 +166,53 @@ def test_weighted_planner_gives_fewer_tokens_to_boundary_heavy_ctas(N):
     assert nseg[heavy] > 10 and toks[heavy] < min(t for c, t in enumerate(toks) if nseg[c] <= 2)
     assert _host_plan(N, sl, 1, 8, seg_cost=-1)[0] == N.SKD_EINVAL
     assert _host_plan(N, sl, 1, 8, seg_cost=70000)[0] == N.SKD_EINVAL
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_aligned_planner_equals_definition(N, seed):
+    rng = np.random.default_rng(500 + seed)
+    B = int(rng.integers(1, 12))
+    hkv = int(rng.choice([1, 2, 8, 12]))
+    n = int(rng.choice([1, 2, 5, 13, 76, 148]))
+    seg_cost = int(rng.choice([0, 1, 8, 40, 1000]))
+    align = int(rng.choice([1, 2, 3, 4, 64]))
+    seqlens = [int(x) for x in rng.integers(0, 3000, size=B)]
+    if seed % 4 == 0:
+        seqlens[int(rng.integers(0, B))] = 0
+    p = _check_against_oracle(N, seqlens, hkv, n, seg_cost=seg_cost, align=align)
+    unit = 16 * align
+    # every split point inside an item is a multiple of the unit; the pieces tile the item
+    for i in range(len(seqlens) * head_groups(hkv)):
+        L = seqlens[i // head_groups(hkv)]
+        pieces = sorted((tb, te) for segs in p["segments"] for it, tb, te, _ in segs if it == i)
+        if L == 0:
+            assert pieces == [(0, 0)]
+            continue
+        assert pieces[0][0] == 0 and pieces[-1][1] == L
+        assert all(a_[1] == b_[0] and a_[1] % unit == 0 for a_, b_ in zip(pieces, pieces[1:]))
+
+
+def test_aligned_planner_one_is_weighted_plan(N):
+    sl = W.draw_seqlens("mla_absorbed").tolist()
+    for c in (0, 8, 40):
+        _, a = _host_plan(N, sl, 1, 76, seg_cost=c)
+        _, b = _host_plan(N, sl, 1, 76, seg_cost=c, align=1)
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("n", [76, 152])
+def test_aligned_planner_reads_no_block_twice(N, n):
+    # 64-token blocks (align 4): the blocks the CTAs touch add up to the blocks of
+    # the batch, and with no segment cost the CTAs' block counts differ by at most one
+    sl = W.draw_seqlens("mla_absorbed").tolist()
+    st, buf = _host_plan(N, sl, 1, n, seg_cost=0, align=4)
+    assert st == 0
+    p = PD.decode(buf)
+    per = [sum((te + 63) // 64 - tb // 64 for _, tb, te, _ in segs) for segs in p["segments"]]
+    assert sum(per) == sum((L + 63) // 64 for L in sl)
+    assert max(per) - min(per) <= 1
+    assert _host_plan(N, sl, 1, n, seg_cost=0, align=0)[0] == N.SKD_EINVAL
+    assert _host_plan(N, sl, 1, n, seg_cost=0, align=65)[0] == N.SKD_EINVAL
 
 
 def test_head_group_rule():

@@ -162,13 +162,14 @@ def test_device_planner_matches_host_planner():
         hkv = int(rng.choice([1, 2, 8]))
         n = int(rng.choice([1, 76, 152]))
         c = int(rng.choice([1, 40, 999]))
+        al = int(rng.choice([1, 3, 4, 64]))
         sl = rng.integers(0, 9000, size=B).astype(np.int32)
         if trial % 3 == 0:
             sl[rng.integers(0, B)] = 0
-        host = skd.plan(sl, hkv, 16, n, seg_cost=c)
-        dev = skd.plan_device(torch.from_numpy(sl).cuda(), hkv, 16, n, seg_cost=c)
+        host = skd.plan(sl, hkv, 16, n, seg_cost=c, align=al)
+        dev = skd.plan_device(torch.from_numpy(sl).cuda(), hkv, 16, n, seg_cost=c, align=al)
         torch.cuda.synchronize()
-        assert torch.equal(host, dev.cpu()), (trial, B, hkv, n, c)
+        assert torch.equal(host, dev.cpu()), (trial, B, hkv, n, c, al)
 
 
 def test_device_plan_drives_the_kernel():

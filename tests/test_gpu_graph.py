@@ -36,9 +36,9 @@ def test_graph_replays_plan_and_attention(case, pdl):
         w = W.make_custom(seed=11, **CASES[case])
         d = Dev(w)
         n = skd.default_ctas(d.shape)
-        c = skd.default_seg_cost(d.shape)
+        c, al = skd.default_seg_cost(d.shape), skd.default_align(d.shape)
         hkv = d.shape.num_kv_heads
-        plan = skd.plan_device(d.sl, hkv, w.page_size, n, seg_cost=c)
+        plan = skd.plan_device(d.sl, hkv, w.page_size, n, seg_cost=c, align=al)
         ws = skd.workspace(d.shape, n)
         kw = dict(scale=w.scale, causal=w.causal, n_ctas=n, shape=d.shape)
         out, lse = skd.decode_attention(d.q, d.k, d.v, d.pt, d.sl, plan, ws, **kw)  # eager, sets attributes
@@ -47,7 +47,7 @@ def test_graph_replays_plan_and_attention(case, pdl):
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.graph(g, stream=s):
-            skd.plan_device(d.sl, hkv, w.page_size, n, out=plan, seg_cost=c)
+            skd.plan_device(d.sl, hkv, w.page_size, n, out=plan, seg_cost=c, align=al)
             skd.decode_attention(d.q, d.k, d.v, d.pt, d.sl, plan, ws, out=out, lse=lse, **kw)
         torch.cuda.current_stream().wait_stream(s)
         out.zero_()

@@ -22,7 +22,8 @@ def _run(w, n_ctas=None, d=None):
     ti = torch.from_numpy(w.topk_idx).cuda()
     tl = torch.from_numpy(w.topk_len).cuda()
     n = skd.default_ctas(d.shape) if n_ctas is None else n_ctas
-    plan = skd.plan(w.topk_len, 1, w.page_size, n, seg_cost=skd.default_seg_cost(d.shape, sparse=True)).cuda()
+    plan = skd.plan(w.topk_len, 1, w.page_size, n, seg_cost=skd.default_seg_cost(d.shape, sparse=True),
+                    align=skd.default_align(d.shape)).cuda()
     ws = skd.workspace(d.shape, n)
     out, lse = skd.decode_attention_sparse(d.q, d.k, d.pt, d.sl, ti, tl, plan, ws, scale=w.scale, n_ctas=n,
                                            shape=d.shape)

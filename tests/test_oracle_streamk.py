@@ -47,11 +47,15 @@ def test_megartp_round_robin_queue_fill():
     assert sorted(q[q >= 0].tolist()) == list(range(g["n_tasks"]))
 
 
-def _brute_force_split(seqlens, hkv, n, granule):
-    """Enumerate every granule of every item, deal contiguous index ranges."""
+def _brute_force_split(seqlens, hkv, n, granule, seg_cost=0):
+    """Enumerate every granule of every item, deal contiguous index ranges.
+    With ``seg_cost``, each non-empty item's granules are preceded by that many
+    placeholder entries that belong to no segment."""
     units = []
     for b, L in enumerate(seqlens):
         for h in range(hkv):
+            if L > 0:
+                units += [(None, None)] * seg_cost
             for u in range(-(-L // granule)):
                 units.append((b * hkv + h, u))
     total = len(units)
@@ -60,7 +64,8 @@ def _brute_force_split(seqlens, hkv, n, granule):
         lo, hi = c * total // n, (c + 1) * total // n
         segs = {}
         for item, u in units[lo:hi]:
-            segs.setdefault(item, []).append(u)
+            if item is not None:
+                segs.setdefault(item, []).append(u)
         row = []
         for item in sorted(segs):
             us = segs[item]
@@ -76,8 +81,8 @@ def test_streamk_split_matches_brute_force_and_invariants(seed):
     B = int(rng.integers(1, 7))
     hkv = int(rng.integers(1, 4))
     n = int(rng.integers(1, 12))
-    granule = int(rng.choice([1, 4, 16]))
-    seqlens = [int(x) for x in rng.integers(0, 120, size=B)]
+    granule = int(rng.choice([1, 4, 16, 64]))
+    seqlens = [int(x) for x in rng.integers(0, 120 if granule < 64 else 700, size=B)]
     if seed % 5 == 0:
         seqlens[0] = 0
     r = S.streamk_split(seqlens, hkv, n, granule)
@@ -107,6 +112,28 @@ def test_streamk_split_matches_brute_force_and_invariants(seed):
     for segs in r["segments"]:
         items = [s[0] for s in segs]
         assert items == sorted(items)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_weighted_split_matches_brute_force(seed):
+    # the segment-cost extension and the coarse cut unit (granule 64 = the MLA
+    # kernel's block): the same split as dealing placeholder entries + granules
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 7))
+    hkv = int(rng.integers(1, 4))
+    n = int(rng.integers(1, 12))
+    granule = int(rng.choice([1, 16, 64]))
+    seg_cost = int(rng.choice([0, 1, 3, 10]))
+    seqlens = [int(x) for x in rng.integers(0, 300 if granule < 64 else 1500, size=B)]
+    if seed % 4 == 0:
+        seqlens[0] = 0
+    r = S.streamk_split(seqlens, hkv, n, granule, seg_cost=seg_cost)
+    bf = _brute_force_split(seqlens, hkv, n, granule, seg_cost=seg_cost)
+    assert [[s for s in segs if s[2] > s[1]] for segs in r["segments"]] == bf
+    assert r["total_granules"] == sum(hkv * (-(-L // granule) + (seg_cost if L else 0)) for L in seqlens)
+    # split points fall on multiples of the granule
+    for i, splits in enumerate(r["item_splits"]):
+        assert all(tb % granule == 0 for _, tb, _ in splits)
 
 
 def test_round_robin_split_deals_whole_items():
