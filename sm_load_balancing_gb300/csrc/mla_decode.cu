@@ -24,7 +24,10 @@
 //     as one 16 KB bulk copy per block;
 //   rank 1 (values): O += P V with M=128, N=2x256, K=64 into its TMEM.
 // Each rank streams the block into its own ring: rank 0 reads it from HBM,
-// rank 1 a few microseconds later, mostly from L2, as its last reader.
+// rank 1 a few microseconds later, mostly from L2, as its last reader. In the
+// sparse (top-k) form a block is 64 listed rows: the ranks share one ring, each
+// gathers part of every block with tile::gather4 and passes it to the partner's
+// stage with one DSMEM bulk copy.
 // The running maximum is kept per row and only moved (with an O rescale on
 // rank 1) when a block's maximum exceeds it by more than 2^8, so p <= 256 and
 // rescales are rare; l and O stay consistent with the same reference maximum.
@@ -43,7 +46,7 @@ namespace {
 
 constexpr int kHeads = 128, kDk = 576, kDv = 512, kBlk = 64;
 // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quarter),
-// (sparse, rank 1) warp 10 forwards its gathered half of each block to rank 0,
+// (sparse, rank 1) warp 10 forwards its gathered part of each block to rank 0,
 // warps 10-11 (rank 0) two more MMA issuers: one thread issues a tcgen05.mma
 // about every 90-120 cycles whatever its size, so the 36 small score MMAs of a
 // block are spread over three issuing warps
@@ -55,13 +58,17 @@ constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kTraceWords = SKD_TRACE_RECORD_BYTES / 8;
 constexpr int kEpiBar = 6;  // named barrier of the 8 epilogue warps of rank 0
 
-// shared memory (offsets are the same in both ranks: TMA multicast and DSMEM
-// stores address the partner's buffers by the local offset)
+// shared memory (offsets are the same in both ranks: multicast commits, DSMEM
+// copies and stores address the partner's buffers by the local offset)
 constexpr uint32_t kChunkBytes = kBlk * 128;       // 64 columns x 64 tokens, bf16, SW128
 constexpr uint32_t kMainBytes = 8 * kChunkBytes;   // value columns [0, 512) of one block
 constexpr uint32_t kPBytes = kHeads * kBlk * 2;    // P of one block: 128 rows x 128 B
 constexpr uint32_t kQuarterP = kPBytes / 4;        // the 32 rows of one epilogue warp
 constexpr uint32_t kQChunkBytes = kHeads * 128;    // Q columns [64 c, 64 c + 64) of all heads, SW128
+// sparse: rank 0 gathers value chunks [0, kGather0) and the rope chunk, rank 1
+// chunks [kGather0, 8), which balances the TMA operations of the two SMs
+constexpr int kGather0 = 4;
+constexpr uint32_t kPart0 = kGather0 * kChunkBytes, kPart1 = (8 - kGather0) * kChunkBytes;
 constexpr uint32_t kOffRing = 0;                   // [kNst][64 KB], both ranks
 constexpr uint32_t kOffRope = kNst * kMainBytes;   // rank 0: [2][8 KB] columns [512, 576)
 constexpr uint32_t kOffStage = kOffRope + 2 * kChunkBytes;  // rank 0: P staging [4 warps][4 KB]
@@ -543,11 +550,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the block is list entries [w0, w0 + 64): tile::gather4 TMA copies
           // bring 4 listed cache rows x 64 columns per op into the 128-byte
           // swizzled stage (16 ops per column chunk, lane c issuing chunk c).
-          // The ring is shared: rank 0 gathers value chunks 0-3 and the rope
-          // chunk, rank 1 chunks 4-7, each into its own stage (barrier KVH),
-          // and each CTA passes its value half to the partner's stage (the
-          // partner's KVF) with one 32 KB bulk copy, so each SM's TMA unit
-          // issues about half of the block's gather operations (plain ones:
+          // The ring is shared: rank 0 gathers value chunks [0, kGather0) and
+          // the rope chunk, rank 1 the other value chunks, each into its own
+          // stage (barrier KVH), and each CTA passes its part to the partner's
+          // stage (the partner's KVF) with one bulk copy, so each SM's TMA unit
+          // issues a similar share of the block's gather operations (plain ones:
           // a multicast gather costs the issuing SM about twice as much).
           // Entries past the list read row 0 of the cache: their scores are
           // masked and rank 1 zeroes their V rows.
@@ -555,8 +562,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = (rank == 0 || g != 1 || cx.wait(B_Q0, 0)) && cx.wait(B_KVE + s, ph ^ 1u) &&
                  (rank == 1 || cx.wait(B_RE0 + (g & 1), uint32_t((g >> 1) & 1) ^ 1u));
             if (ok) {
-              ptx::mbar_arrive_expect_tx(cx.bar(B_KVH + s), rank == 0 ? kMainBytes / 2 + kChunkBytes : kMainBytes / 2);
-              ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), kMainBytes / 2);
+              ptx::mbar_arrive_expect_tx(cx.bar(B_KVH + s), rank == 0 ? kPart0 + kChunkBytes : kPart1);
+              ptx::mbar_arrive_expect_tx(cx.bar(B_KVF + s), rank == 0 ? kPart1 : kPart0);
               misc[4] = (misc[4] ^ (1u << s)) | (256u << s);
             }
           }
@@ -564,8 +571,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           const uint32_t ring = cx.sbase + kOffRing + s * kMainBytes;
           const uint32_t rope = cx.sbase + kOffRope + (g & 1) * kChunkBytes;
-          // this rank's chunks: rank 0 lanes 0-3 (+ lane 8: rope), rank 1 lanes 4-7
-          const bool mine = rank == 0 ? (lane < 4 || lane == 8) : (lane >= 4 && lane < 8);
+          // this rank's chunks: lane c issues chunk c (lane 8: rope, rank 0)
+          const bool mine = rank == 0 ? (lane < kGather0 || lane == 8) : (lane >= kGather0 && lane < 8);
 #pragma unroll 1
           for (int i = 0; i < kBlk / 4; ++i) {
             int r4[4];
@@ -607,7 +614,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || (rank == 0 && warp >= 10)) {
     // ============================ MMA issuers ================================
     if (lane == 0) {
-      const uint32_t half_src = cx.sbase + kOffRing;  // rank 0's value half: chunks 0-3 of a stage
+      const uint32_t part_src = cx.sbase + kOffRing;  // rank 0's value part: chunks [0, kGather0) of a stage
       int g = 0;
       bool ok = true;
       if (rank == 0) {
@@ -649,14 +656,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int j = 0; j < nb && ok; ++j, ++g, ++m) {
             const int s = m % kNst;
             if (sparse && qi == 0) {
-              // issuer 0 passes rank 0's gathered value half to rank 1 as soon
+              // issuer 0 passes rank 0's gathered value part to rank 1 as soon
               // as it has landed (it waits for this stage anyway)
               if (!cx.wait(B_KVH + s, uint32_t(m / kNst) & 1u)) {
                 ok = false;
                 break;
               }
-              const uint32_t src = half_src + uint32_t(s) * kMainBytes;
-              bulk_s2s(cx.peer_addr(src), src, kMainBytes / 2, cx.peer_addr(cx.bar(B_KVF + s)));
+              const uint32_t src = part_src + uint32_t(s) * kMainBytes;
+              bulk_s2s(cx.peer_addr(src), src, kPart0, cx.peer_addr(cx.bar(B_KVF + s)));
               bulk_commit();
             }
             const uint32_t par = uint32_t(m / kNst) & 1u;
@@ -1202,8 +1209,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     (void)ok;
   } else if (sparse && rank == 1 && warp == 10) {
-    // ======== sparse, rank 1: pass the gathered value half (chunks 4-7) to rank 0 ========
-    // (one 32 KB bulk copy per block into rank 0's stage, counted on its KVF, as
+    // ======== sparse, rank 1: pass the gathered value part (chunks [kGather0, 8)) to rank 0 ========
+    // (one bulk copy per block into rank 0's stage, counted on its KVF, as
     // soon as it landed here: rank 0 needs it before P, and so before rank 1's PV).
     // This warp releases every fill of the ring here, the copied ones once the
     // copy has read them, so no barrier it waits on can run two phases ahead.
@@ -1227,8 +1234,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = cx.wait(B_KVH + s, (hp >> s) & 1u);
           if (!ok) break;
           hp ^= 1u << s;
-          const uint32_t src = cx.sbase + kOffRing + uint32_t(s) * kMainBytes + kMainBytes / 2;
-          bulk_s2s(cx.peer_addr(src), src, kMainBytes / 2, cx.peer_addr(cx.bar(B_KVF + s)));
+          const uint32_t src = cx.sbase + kOffRing + uint32_t(s) * kMainBytes + kPart0;
+          bulk_s2s(cx.peer_addr(src), src, kPart1, cx.peer_addr(cx.bar(B_KVF + s)));
           bulk_commit();
           bulk_wait_read0();
           ptx::mbar_arrive(cx.bar(B_KVE + s));
