@@ -440,7 +440,24 @@ def run_ours(a):
             tl_h = torch.from_numpy(w.topk_len).pin_memory()
             ti_d, tl_d = torch.empty_like(ti), torch.empty_like(tl)
 
+        # the serving-loop API: one captured step (H2D, device planner, decode, D2H)
+        step = None
+        if prefix is None and a.mode == "streamk":
+            from sm_load_balancing_gb300.step import DecodeStep
+            step = DecodeStep(q, k, v, w.page_table.shape[1], scale=w.scale, causal=w.causal,
+                              topk=int(w.topk_idx.shape[1]) if sparse else None, n_ctas=n, seg_cost=seg_cost,
+                              align=align)
+            step.q_host.copy_(q_h)
+            step.page_table_host.copy_(pt_h)
+            step.seqlens_host.copy_(sl_h)
+            if sparse:
+                step.topk_idx_host.copy_(ti_h)
+                step.topk_len_host.copy_(tl_h)
+
         def e2e_step():
+            if step is not None:
+                step.run()
+                return
             lens_h = tl_h if sparse else sl_h
             p = skd.plan(lens_h, shape.num_kv_heads, w.page_size, n, a.mode, seg_cost=seg_cost,
                          align=align)  # host planner
@@ -477,18 +494,24 @@ def run_ours(a):
             t = torch.tensor([t_e2e], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             t_e2e = float(t.item())
-        h2d = q_h.numel() * 2 + pt_h.numel() * 4 + sl_h.numel() * 4 + plan_pin.numel() * 4
-        if sparse:
-            h2d += ti_h.numel() * 4 + tl_h.numel() * 4
-        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        if step is not None:
+            h2d, d2h = step.host_to_device_bytes(), step.device_to_host_bytes()
+            note = ("DecodeStep.run(): one CUDA graph replay of pinned H2D of q/page table/seqlens"
+                    + ("/top-k lists" if sparse else "") + " + device planner + kernel + D2H of out/lse, "
+                    "then a host wait; KV cache resident")
+        else:
+            h2d = q_h.numel() * 2 + pt_h.numel() * 4 + sl_h.numel() * 4 + plan_pin.numel() * 4
+            if sparse:
+                h2d += ti_h.numel() * 4 + tl_h.numel() * 4
+            d2h = out_h.numel() * 2 + lse_h.numel() * 4
+            note = ("host planner + pinned H2D of q/seqlens/page table/plan" + ("/top-k lists" if sparse else "")
+                    + " + kernel + D2H of out/lse; KV cache resident"
+                    + ("; shared prefix: its layouts and plans are prepared once, outside the loop"
+                       if prefix is not None else ""))
         e2e = {"value": world * alg_bytes / t_e2e / 1e12, "unit": "TB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "us_per_step": t_e2e * 1e6, "steps": n_e2e,
-               "note": "host planner + pinned H2D of q/seqlens/page table/plan" + ("/top-k lists" if sparse else "")
-                       + " + kernel + D2H of out/lse; KV cache resident"
-                       + ("; shared prefix: its layouts and plans are prepared once, outside the loop"
-                          if prefix is not None else "")}
-        if skd.read_error(ws) != 0:
+               "us_per_step": t_e2e * 1e6, "steps": n_e2e, "note": note}
+        if skd.read_error(ws) != 0 or (step is not None and step.error() != 0):
             raise RuntimeError("device error in e2e loop")
 
     peak, peak_src = _measured_hbm_peak()
