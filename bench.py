@@ -6,11 +6,20 @@ Stream-K plan + one persistent kernel). Default workload: the Llama-3-8B-shaped
 GQA decode batch (B=32, 32 q / 8 kv heads, D=128, L ~ U[512, 8192], P=16).
 
   value   algorithmic bytes / device time (CUDA events on the launching stream),
-          inputs resident in HBM; KV (~570 MB) is larger than L2, so no flush
-  e2e     the same metric through the public API with host buffers: per step the
-          host planner runs, q / seqlens / page table / plan are copied from
-          pinned host memory, and out / lse are copied back (KV cache resident)
-  roofline / cpu_baseline / clocks: see the design doc (measurement section)
+          inputs resident in HBM; when a step reads less than twice L2's size a
+          256 MB write evicts L2 before every step (each step then has its own
+          events), otherwise the steps run back to back between two events
+  e2e     the same metric through the public API with host buffers, KV cache
+          resident: for Stream-K plans DecodeStep.run() (one graph replay of the
+          pinned H2D copies of q / page table / seqlens, the device planner, the
+          kernel and the D2H copies of out / lse, then a host wait); otherwise
+          the eager calls with the host planner and the plan copied too
+  roofline  achieved = algorithmic bytes / mean kernel time against the measured
+          HBM copy bandwidth (MEASURED_PEAKS.json, else a 6.8 TB/s fallback);
+          traffic = ncu DRAM bytes per launch recorded in profiles/, reported
+          only while the kernel source hash matches the one captured
+  cpu_baseline  the fp64 oracle on a bounded sample, on all host cores
+  clocks  nvidia-smi samples taken during the timed region
 
 --impl reference times the fp64 CPU oracle on the host cores instead.
 Multi-GPU (torchrun): every rank runs an independent replica (weak scaling, no
