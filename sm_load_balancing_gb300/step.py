@@ -38,13 +38,21 @@ class DecodeStep:
                  n_ctas: Optional[int] = None, seg_cost: Optional[int] = None, align: Optional[int] = None):
         from . import (decode_attention, decode_attention_sparse, default_align, default_ctas, default_seg_cost,
                        make_shape, plan_bytes, plan_device, workspace)
+        if q_like.dim() != 4 or q_like.dtype != torch.bfloat16:
+            raise ValueError("q_like must be a bf16 tensor [B, T, Hq, Dk]")
+        if k_pages.device.type != "cuda" or k_pages.dtype != torch.bfloat16:
+            raise ValueError("k_pages must be a CUDA bf16 tensor (the resident cache)")
+        if v_pages is not None and (v_pages.device != k_pages.device or v_pages.dtype != torch.bfloat16):
+            raise ValueError("v_pages must be a bf16 tensor on k_pages' device")
+        if int(max_pages) < 1:
+            raise ValueError("max_pages must be at least 1")
         dev = k_pages.device
         B, T, Hq = int(q_like.shape[0]), int(q_like.shape[1]), int(q_like.shape[2])
         if causal is None:
             causal = T > 1
         self.sparse = topk is not None
-        if self.sparse and v_pages is not None:
-            raise ValueError("the sparse form is absorbed MLA: v_pages must be None")
+        if self.sparse and (v_pages is not None or causal or int(topk) < 1):
+            raise ValueError("the sparse form is absorbed MLA without a causal mask (v_pages None, topk >= 1)")
         pin = dict(pin_memory=True)
         # pinned host inputs and outputs (the caller's side of the step)
         self.q_host = torch.zeros(tuple(q_like.shape), dtype=torch.bfloat16, **pin)
