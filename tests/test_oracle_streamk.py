@@ -139,3 +139,44 @@ def test_weighted_split_matches_brute_force(seed):
 def test_round_robin_split_deals_whole_items():
     r = S.round_robin_split([5, 0, 9], 2, 4)
     assert r["segments"] == [[(0, 0, 5), (4, 0, 9)], [(1, 0, 5), (5, 0, 9)], [(2, 0, 0)], [(3, 0, 0)]]
+
+
+def test_fixed_split_hand_example():
+    # 3 items on 7 CTAs: S = 7 // 3 = 2 splits per item. Item 0 has 7 granules
+    # (100 tokens): granules [0, 3) and [3, 7) -> tokens [0, 48) and [48, 100);
+    # item 1 is empty: one empty piece; item 2 has 3 granules: [0, 1), [1, 3) ->
+    # tokens [0, 16), [16, 40). The five pieces go to CTAs 0..4 in that order.
+    r = S.fixed_split([100, 0, 40], 1, 7)
+    assert r["splits_per_item"] == 2
+    assert r["item_splits"] == [[(0, 48), (48, 100)], [(0, 0)], [(0, 16), (16, 40)]]
+    assert r["segments"] == [[(0, 0, 48)], [(0, 48, 100)], [(1, 0, 0)], [(2, 0, 16)], [(2, 16, 40)], [], []]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_fixed_split_properties(seed):
+    rng = np.random.default_rng(2000 + seed)
+    B = int(rng.integers(1, 9))
+    hkv = int(rng.integers(1, 4))
+    n = int(rng.integers(1, 40))
+    seqlens = [int(x) for x in rng.integers(0, 500, size=B)]
+    r = S.fixed_split(seqlens, hkv, n)
+    items = B * hkv
+    assert r["splits_per_item"] == max(1, n // items)
+    flat = []
+    for i, parts in enumerate(r["item_splits"]):
+        L = seqlens[i // hkv]
+        g = -(-L // 16)
+        assert len(parts) == max(1, min(r["splits_per_item"], g))
+        assert parts[0][0] == 0 and parts[-1][1] == L
+        assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
+        if g:
+            sizes = [-(-(te - tb) // 16) for tb, te in parts]  # granules per piece
+            assert max(sizes) - min(sizes) <= 1 and sum(sizes) == g
+            assert all(tb % 16 == 0 for tb, _ in parts)
+        flat += [(i, tb, te) for tb, te in parts]
+    # piece j of the (item, split) order goes to CTA j mod n
+    for j, seg in enumerate(flat):
+        assert seg in r["segments"][j % n]
+    assert sum(len(s) for s in r["segments"]) == len(flat)
+    if items <= n:
+        assert all(len(s) <= 1 for s in r["segments"])
